@@ -1,0 +1,417 @@
+#!/usr/bin/env python3
+"""Throughput of the blockwise-FP8 routed-MoE layer on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl native|reference]
+
+A step is one pass of the whole layer (router, permutation, gate/up + SwiGLU,
+down, combine) over one synthetic batch already resident in HBM.  The L2 is
+flushed (a 256 MiB memset, twice the 129 MB L2) before every step and the
+step is timed with CUDA events on the launching stream.  The default workload
+is the OLMoE-shaped decode batch of 8 tokens (H=2048, E=64, top-8, I=1024).
+
+Printed: ONE JSON line.  Besides the contract keys it carries
+  roofline      : the dominant kernel's algorithmic bytes (or FLOPs) per launch
+                  over its CUDA-event duration, against MEASURED_PEAKS.json;
+  layer         : the same for the whole step (selected-expert bytes / step);
+  cpu_baseline  : the f64 CPU oracle on a bounded sample of the workload;
+  e2e           : the metric through the host-buffer C-ABI entry point;
+  clocks        : nvidia-smi samples taken during the timed region.
+``--impl reference`` times the CPU oracle as the reference arm instead.
+Under torchrun (N > 1) every rank runs an independent replica.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill FP8 TFLOP/s vs roofline"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = "olmoe_decode_T8"
+FLUSH_BYTES = 256 << 20
+FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput on GB300 (4.5 / 2.25 PFLOP/s)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), \
+        int(os.environ.get("WORLD_SIZE", 1))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def selected_bytes(fam, counts) -> dict:
+    """Algorithmic bytes of one step: every active expert's codes and scales
+    once, the router, the activations in and out."""
+    H, I, E = fam.hidden, fam.inter, fam.n_experts
+    n_act = int((np.asarray(counts) > 0).sum())
+    w13 = 2 * I * H + 4 * (2 * I // 128) * (H // 128)
+    w2 = H * I + 4 * (H // 128) * (I // 128)
+    return dict(n_active=n_act, w13=n_act * w13, w2=n_act * w2, router=E * H * 4)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.device = device
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{device}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.device), "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ oracle timing
+
+_ORACLE_CHILD = r"""
+import json, sys, time, os
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import workloads as W, oracle
+fam, T = W.parse_workload(sys.argv[2])
+budget, max_tokens = float(sys.argv[3]), int(sys.argv[4])
+w = W.make_weights(fam)
+x = W.make_x(fam, T)
+tokens = np.arange(min(T, max_tokens))
+t0 = time.perf_counter(); n = 0
+while True:
+    oracle.moe_forward(x, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2, fam.top_k,
+                       tokens=tokens)
+    n += 1
+    el = time.perf_counter() - t0
+    if el >= budget or n >= 1000:
+        break
+print(json.dumps({"seconds": el, "reps": n, "tokens_per_rep": int(tokens.size), "T": T}))
+"""
+
+
+def oracle_rate(workload: str, seconds: float, max_tokens: int = 64) -> dict:
+    """Oracle tokens/s on the host cores, in a fresh single-threaded process.
+
+    Sample: the whole routing of the batch plus the expert FFN and combine of
+    its first min(T, max_tokens) tokens, repeated for about `seconds`."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", _ORACLE_CHILD, ROOT, workload, str(seconds),
+                        str(max_tokens)], capture_output=True, text=True, env=env, timeout=1800)
+    if r.returncode != 0:
+        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    rate = d["reps"] * d["tokens_per_rep"] / d["seconds"]
+    return dict(value=rate, unit=UNIT, cores=1, kind="oracle",
+                sample=(f"{d['reps']} oracle passes over {workload}: routing of all {d['T']} tokens "
+                        f"+ experts and combine of {d['tokens_per_rep']} tokens, f64, "
+                        f"{d['seconds']:.1f} s"), seconds=d["seconds"])
+
+
+# ------------------------------------------------------------------ native arm
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_routed_expert_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(f"{kernel}/{workload}")
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def run_native(args, rank, local_rank, world):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from fp8_routed_expert_gb300 import MoELayer
+
+    fam, T = W.parse_workload(args.workload)
+    k = fam.top_k
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.make_weights(fam)
+    xb = W.make_x(fam, T)
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    rw, rb = g(w.router_w), (None if w.router_bias is None else g(w.router_bias))
+    w13, s13, w2, s2 = g(w.w13), g(w.s13), g(w.w2), g(w.s2)
+    x = torch.from_numpy(xb.astype(np.int16)).view(torch.bfloat16).to(dev)
+    out = torch.empty_like(x)
+    layer = MoELayer(T, fam.hidden, fam.n_experts, fam.inter, k, local_rank)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    decode = T <= 64
+    dominant = "gate_up"
+
+    def step():
+        layer.forward(x, rw, rb, w13, s13, w2, s2, k, out=out, stream=stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    assert layer.status() == 0
+    counts = layer.routing(T, k)["counts"].cpu().numpy()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    layer.set_timing([dominant])
+    n0 = layer.launch_count()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local_rank) as clk:
+        t_wall = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+        t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    launches = layer.launch_count() - n0
+    dom_ms, dom_n = layer.kernel_time(dominant)
+    layer.set_timing(())
+    assert layer.status() == 0
+    step_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
+
+    # end to end through the host-buffer entry point (pinned buffers)
+    xh = torch.from_numpy(xb.astype(np.int16)).view(torch.bfloat16).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    for _ in range(3):
+        layer.forward_host(xh, rw, rb, w13, s13, w2, s2, k, oh, stream=stream)
+    K2 = max(1, min(K, 500))
+    e2e_ms = []
+    for _ in range(K2):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        layer.forward_host(xh, rw, rb, w13, s13, w2, s2, k, oh, stream=stream)
+        b.record(stream)
+        b.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e_step = sum(e2e_ms) / K2
+
+    stats = torch.tensor([step_ms, e2e_step], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(stats, op=torch.distributed.ReduceOp.MAX)
+    step_ms, e2e_step = stats.tolist()
+    if rank != 0:
+        return None
+
+    hbm, bf16, bf16_sus, src = peaks()
+    sb = selected_bytes(fam, counts)
+    P = T * k
+    dom_s = dom_ms / max(dom_n, 1) / 1e3
+    if decode:
+        dom_bytes = sb["w13"] + T * fam.hidden * 2 + P * fam.inter * 4
+        achieved = dom_bytes / dom_s / 1e9
+        roof = dict(bound="hbm", achieved=achieved, peak=hbm, unit="GB/s", frac=achieved / hbm,
+                    traffic=profiled_traffic(dominant, args.workload),
+                    kernel="gate_up_swiglu (grouped GEMV)", algorithmic_bytes=dom_bytes,
+                    avg_launch_us=dom_s * 1e6, peak_source=f"hbm_gbs, {src}")
+    else:
+        flops = 2.0 * P * fam.hidden * 2 * fam.inter
+        fp8_peak = bf16 * FP8_PER_BF16
+        achieved = flops / dom_s / 1e12
+        roof = dict(bound="tensor", achieved=achieved, peak=fp8_peak, unit="TFLOP/s",
+                    frac=achieved / fp8_peak, traffic=profiled_traffic(dominant, args.workload),
+                    kernel="gate_up_swiglu (grouped GEMM)", algorithmic_flops=flops,
+                    avg_launch_us=dom_s * 1e6,
+                    peak_source=f"bf16_tflops x {FP8_PER_BF16} (nominal fp8/bf16), {src}")
+    layer_bytes = sb["w13"] + sb["w2"] + sb["router"] + 2 * T * fam.hidden * 2
+    layer_gbs = layer_bytes / (step_ms / 1e3) / 1e9
+    expert_flops = 6.0 * P * fam.hidden * fam.inter
+    value = world * T / (step_ms / 1e3)
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 weights x f16 activations, f32 accumulate" if decode or True else "",
+        "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised to "
+                "e4m3 per 128x128 block)",
+        "config": {"workload": args.workload, "tokens": T, "hidden": fam.hidden,
+                   "experts": fam.n_experts, "top_k": k, "inter": fam.inter,
+                   "active_experts": sb["n_active"],
+                   "l2": "flushed before every step (256 MiB memset)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "layer": {"bytes": layer_bytes, "gbs": layer_gbs, "hbm_frac": layer_gbs / hbm,
+                  "expert_tflops": expert_flops / (step_ms / 1e3) / 1e12},
+        "gpu_launches": int(launches),
+        "e2e": {"value": world * T / (e2e_step / 1e3), "unit": UNIT,
+                "h2d_bytes_per_step": T * fam.hidden * 2, "d2h_bytes_per_step": T * fam.hidden * 2,
+                "ms_per_step": e2e_step},
+        "wall_s_timed_region": t_wall,
+        "clocks": clk.summary(),
+    }
+    return res
+
+
+def main():
+    args = parse()
+    rank, local_rank, world = dist_env()
+    fam, T = W.parse_workload(args.workload)
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        steps = args.steps if args.steps is not None else 3
+        warm = args.warmup if args.warmup is not None else 1
+        r = oracle_reference_arm(args.workload, steps, warm)
+        r.update(n_gpus=args.gpus, steps=steps, warmup=warm)
+        print(json.dumps(r))
+        return 0
+
+    if args.steps is None:
+        args.steps = 3000 if T <= 64 else 200
+    if args.warmup is None:
+        args.warmup = 20
+    args.warmup = max(args.warmup, 3)
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = run_native(args, rank, local_rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = oracle_rate(args.workload, args.cpu_seconds)
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+_REF_STEP = r"""
+import json, sys, time
+sys.path.insert(0, sys.argv[1])
+import numpy as np
+import workloads as W, oracle
+fam, T = W.parse_workload(sys.argv[2])
+steps, warm, max_tokens = int(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5])
+w = W.make_weights(fam)
+x = W.make_x(fam, T)
+tokens = np.arange(min(T, max_tokens))
+times = []
+for i in range(warm + steps):
+    t0 = time.perf_counter()
+    oracle.moe_forward(x, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2, fam.top_k,
+                       tokens=tokens)
+    if i >= warm:
+        times.append(time.perf_counter() - t0)
+print(json.dumps({"times": times, "tokens": int(tokens.size), "T": T}))
+"""
+
+
+def oracle_reference_arm(workload: str, steps: int, warmup: int, max_tokens: int = 64) -> dict:
+    """The reference arm: the CPU oracle timed on the host cores, one bounded
+    sample of the workload per step (routing of the whole batch, experts and
+    combine of its first min(T, 64) tokens)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, "-c", _REF_STEP, ROOT, workload, str(steps), str(warmup),
+                        str(max_tokens)], capture_output=True, text=True, env=env, timeout=3600)
+    if r.returncode != 0:
+        return {"impl": "reference", "unavailable": "oracle run failed: " + r.stderr[-300:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    sec = sum(d["times"]) / len(d["times"])
+    value = d["tokens"] / sec
+    fam, T = W.parse_workload(workload)
+    sample = (f"per step: routing of all {d['T']} tokens + experts and combine of "
+              f"{d['tokens']} tokens of {workload}, f64 oracle, 1 thread")
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": workload, "tokens": T, "hidden": fam.hidden,
+                       "experts": fam.n_experts, "top_k": fam.top_k, "inter": fam.inter},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,45 @@
+// Internal launchers of the layer's kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fp8moe {
+
+// T at or below which the router uses one warp per expert row; above it, the
+// tiled kernel.
+constexpr int64_t kRouterWarpMaxT = 64;
+// Rows of one grouped-GEMM tile (tile list granularity).
+constexpr int kTileM = 128;
+
+int router_chain_depth(int64_t T, int64_t H);
+cudaError_t launch_router_logits(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
+                                 int64_t H, float *logits, float *wnorm, cudaStream_t s);
+size_t router_select_smem(int64_t E);
+cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float *W,
+                                 const float *bias, int64_t E, int64_t H, int k,
+                                 const float *logits, const float *wnorm, float gamma_d,
+                                 int32_t *idx, float *wts, __half *x16, float *xscale, int *err,
+                                 cudaStream_t s);
+
+size_t permute_smem(int E);
+cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int tile_m, int32_t *counts,
+                           int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *active,
+                           int32_t *n_active, int32_t *tile_offsets, uint32_t *pos_max, int *err,
+                           cudaStream_t s);
+
+cudaError_t launch_gemv13(const uint8_t *w13, const float *s13, const __half *x16,
+                          const float *xscale, const int32_t *counts, const int32_t *offsets,
+                          const int32_t *perm, const int32_t *active, const int32_t *n_active,
+                          int k, int64_t H, int64_t I, float *h, uint32_t *hmax, int64_t max_items,
+                          int wide_tokens, int grid_cap, cudaStream_t s);
+cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, const uint32_t *hmax,
+                         const int32_t *counts, const int32_t *offsets, const int32_t *active,
+                         const int32_t *n_active, int64_t H, int64_t I, float *y,
+                         int64_t max_items, int wide_tokens, int grid_cap, cudaStream_t s);
+cudaError_t launch_combine(const float *y, const int32_t *inv, const float *wts, int64_t T, int k,
+                           int64_t H, __nv_bfloat16 *out, cudaStream_t s);
+
+}  // namespace fp8moe

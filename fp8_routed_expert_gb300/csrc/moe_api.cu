@@ -1,0 +1,407 @@
+// C ABI of the routed-MoE layer: context, workspace, argument checks and the
+// order of kernel launches.  See include/fp8moe.h for the contract.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "fp8moe.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace fp8moe;
+
+namespace {
+
+constexpr int64_t kGemvMaxT = 64;  // MOE_PATH_AUTO: GEMV path up to this T
+
+struct TimingRec {
+  cudaEvent_t a, b;
+  int kernel;
+};
+
+}  // namespace
+
+struct moe_ctx {
+  moe_config cfg{};
+  int sms = 0;
+  char *ws = nullptr;
+  size_t ws_bytes = 0;
+  // workspace views
+  float *logits = nullptr, *wnorm = nullptr, *wts = nullptr, *xscale = nullptr;
+  float *h = nullptr, *y = nullptr;
+  int32_t *idx = nullptr, *counts = nullptr, *offsets = nullptr, *perm = nullptr, *inv = nullptr;
+  int32_t *active = nullptr, *n_active = nullptr, *tile_offsets = nullptr;
+  uint32_t *hmax = nullptr;
+  __half *x16 = nullptr;
+  __nv_bfloat16 *xin = nullptr, *xout = nullptr;  // staging for the host-buffer entry point
+  int *err = nullptr;
+  int path = MOE_PATH_AUTO;
+  // last forward
+  int64_t last_T = 0;
+  int last_k = 0;
+  cudaStream_t last_stream = nullptr;
+  // timing
+  int timing = 0;  // bit mask of timed kernels
+  int64_t n_launches = 0;
+  std::vector<TimingRec> pending;
+  std::vector<cudaEvent_t> spare;
+  double total_ms[MOE_K_COUNT] = {};
+  int64_t launches[MOE_K_COUNT] = {};
+};
+
+namespace {
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_config(const moe_config *c) {
+  if (c->max_tokens <= 0 || c->hidden <= 0 || c->inter <= 0 || c->n_experts <= 0)
+    return MOE_ERR_SHAPE;
+  if (c->hidden % 128 != 0 || c->inter % 128 != 0) return MOE_ERR_SHAPE;
+  if (c->hidden > 65536 || c->inter > 65536 || c->n_experts > 1024) return MOE_ERR_SHAPE;
+  if (c->max_top_k < 1 || c->max_top_k > 32 || c->max_top_k > c->n_experts) return MOE_ERR_SHAPE;
+  if (c->max_tokens > (int64_t)(INT32_MAX / 2) / c->max_top_k) return MOE_ERR_SHAPE;
+  if (c->device < 0) return MOE_ERR_ARG;
+  return MOE_OK;
+}
+
+float router_gamma(int64_t T, int64_t H) {
+  const double u = std::ldexp(1.0, -24);
+  const double d = (double)router_chain_depth(T, H);
+  const double g = d * u / (1.0 - d * u);
+  return std::nextafter((float)(g * (1.0 + 1e-6)), INFINITY);
+}
+
+// Events around one kernel launch when timing is on.
+struct Timed {
+  moe_ctx *c;
+  int kernel;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr, b = nullptr;
+  bool on;
+  Timed(moe_ctx *ctx, int k, cudaStream_t st) : c(ctx), kernel(k), s(st) {
+    c->n_launches += 1;
+    on = (c->timing >> k) & 1;
+    if (!on) return;
+    a = take();
+    b = take();
+    if (a) cudaEventRecord(a, s);
+  }
+  cudaEvent_t take() {
+    if (!c->spare.empty()) {
+      cudaEvent_t e = c->spare.back();
+      c->spare.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+  }
+  ~Timed() {
+    if (!on || !a || !b) return;
+    cudaEventRecord(b, s);
+    c->pending.push_back({a, b, kernel});
+  }
+};
+
+void drain_timing(moe_ctx *c) {
+  for (auto &r : c->pending) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      c->total_ms[r.kernel] += ms;
+      c->launches[r.kernel] += 1;
+    }
+    c->spare.push_back(r.a);
+    c->spare.push_back(r.b);
+  }
+  c->pending.clear();
+}
+
+#define CUDA_TRY(expr)                          \
+  do {                                          \
+    cudaError_t e_ = (expr);                    \
+    if (e_ != cudaSuccess) return MOE_ERR_CUDA; \
+  } while (0)
+
+int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw,
+                   const float *rb, const uint8_t *w13, const float *s13, const uint8_t *w2,
+                   const float *s2, int k, __nv_bfloat16 *out, cudaStream_t s) {
+  const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, I = c->cfg.inter;
+  const int64_t P = T * k;
+  const int path = c->path != MOE_PATH_AUTO ? c->path : (T <= kGemvMaxT ? MOE_PATH_GEMV : MOE_PATH_GEMM);
+  const int wide = (path == MOE_PATH_GEMM || T > kGemvMaxT) ? 1 : 0;
+  const int64_t max_active = P < E ? P : E;
+  {
+    Timed tm(c, MOE_K_ROUTER_LOGITS, s);
+    CUDA_TRY(launch_router_logits(x, T, rw, E, H, c->logits, c->wnorm, s));
+  }
+  {
+    Timed tm(c, MOE_K_ROUTER_SELECT, s);
+    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm,
+                                  router_gamma(T, H), c->idx, c->wts, c->x16, c->xscale, c->err, s));
+  }
+  {
+    Timed tm(c, MOE_K_PERMUTE, s);
+    CUDA_TRY(launch_permute(c->idx, P, (int)E, kTileM, c->counts, c->offsets, c->perm, c->inv,
+                            c->active, c->n_active, c->tile_offsets, c->hmax, c->err, s));
+  }
+  {
+    Timed tm(c, MOE_K_GATE_UP, s);
+    CUDA_TRY(launch_gemv13(w13, s13, c->x16, c->xscale, c->counts, c->offsets, c->perm, c->active,
+                           c->n_active, k, H, I, c->h, c->hmax, max_active * (I / 32), wide,
+                           c->sms * 4, s));
+  }
+  {
+    Timed tm(c, MOE_K_DOWN, s);
+    CUDA_TRY(launch_gemv2(w2, s2, c->h, c->hmax, c->counts, c->offsets, c->active, c->n_active, H,
+                          I, c->y, max_active * (H / 64), wide, c->sms * 4, s));
+  }
+  {
+    Timed tm(c, MOE_K_COMBINE, s);
+    CUDA_TRY(launch_combine(c->y, c->inv, c->wts, T, k, H, out, s));
+  }
+  c->last_T = T;
+  c->last_k = k;
+  c->last_stream = s;
+  if (c->timing && c->pending.size() > 16384) drain_timing(c);
+  return MOE_OK;
+}
+
+int check_forward_args(moe_ctx *c, const void *hidden, int64_t T, const float *rw,
+                       const float *rb, const uint8_t *w13, const float *s13, const uint8_t *w2,
+                       const float *s2, int32_t k, const void *out) {
+  if (c == nullptr) return MOE_ERR_ARG;
+  if (T < 0) return MOE_ERR_ARG;
+  if (T > c->cfg.max_tokens) return MOE_ERR_SHAPE;
+  if (k < 1 || k > c->cfg.max_top_k || k > c->cfg.n_experts) return MOE_ERR_SHAPE;
+  if (T == 0) return MOE_OK;
+  if (!hidden || !rw || !w13 || !s13 || !w2 || !s2 || !out) return MOE_ERR_ARG;
+  if (!aligned(hidden, 16) || !aligned(rw, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
+      !aligned(out, 16) || !aligned(s13, 4) || !aligned(s2, 4) || (rb && !aligned(rb, 4)))
+    return MOE_ERR_ALIGN;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_ARG: return "invalid argument";
+    case MOE_ERR_SHAPE: return "unsupported shape (H, I multiples of 128; k in [1, min(E, max_top_k)]; T <= max_tokens)";
+    case MOE_ERR_ALIGN: return "misaligned pointer";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait gave up";
+    case MOE_ERR_NOMEM: return "workspace allocation failed";
+    case MOE_ERR_UNSUPPORTED: return "device is not compute capability 10.3 (sm_103a)";
+    case MOE_ERR_NONFINITE: return "a router logit was NaN or infinite";
+    case MOE_ERR_DEVICE: return "device-side consistency check failed";
+    default: return "unknown error";
+  }
+}
+
+const char *moe_kernel_name(int kernel) {
+  static const char *names[MOE_K_COUNT] = {"router_logits", "router_select", "permute",
+                                           "gate_up_swiglu", "down", "combine", "act_quant"};
+  return (kernel >= 0 && kernel < MOE_K_COUNT) ? names[kernel] : "unknown";
+}
+
+int moe_init(moe_ctx **out, const moe_config *cfg) {
+  if (out == nullptr) return MOE_ERR_ARG;
+  *out = nullptr;
+  if (cfg == nullptr) return MOE_ERR_ARG;
+  int rc = check_config(cfg);
+  if (rc != MOE_OK) return rc;
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev <= 0) return MOE_ERR_CUDA;
+  if (cfg->device >= ndev) return MOE_ERR_ARG;
+  if (cudaSetDevice(cfg->device) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!(prop.major == 10 && prop.minor == 3)) return MOE_ERR_UNSUPPORTED;
+
+  moe_ctx *c = new (std::nothrow) moe_ctx();
+  if (c == nullptr) return MOE_ERR_NOMEM;
+  c->cfg = *cfg;
+  c->sms = prop.multiProcessorCount;
+
+  const int64_t Tm = cfg->max_tokens, E = cfg->n_experts, H = cfg->hidden, I = cfg->inter;
+  const int64_t Pm = Tm * cfg->max_top_k;
+  struct Slot {
+    void **p;
+    size_t bytes;
+  } slots[] = {
+      {(void **)&c->logits, (size_t)(Tm * E) * 4},
+      {(void **)&c->wnorm, (size_t)E * 4},
+      {(void **)&c->idx, (size_t)Pm * 4},
+      {(void **)&c->wts, (size_t)Pm * 4},
+      {(void **)&c->counts, (size_t)E * 4},
+      {(void **)&c->offsets, (size_t)(E + 1) * 4},
+      {(void **)&c->perm, (size_t)Pm * 4},
+      {(void **)&c->inv, (size_t)Pm * 4},
+      {(void **)&c->active, (size_t)E * 4},
+      {(void **)&c->n_active, 16},
+      {(void **)&c->tile_offsets, (size_t)(E + 1) * 4},
+      {(void **)&c->hmax, (size_t)Pm * 4},
+      {(void **)&c->x16, (size_t)(Tm * H) * 2},
+      {(void **)&c->xscale, (size_t)Tm * 4},
+      {(void **)&c->h, (size_t)(Pm * I) * 4},
+      {(void **)&c->y, (size_t)(Pm * H) * 4},
+      {(void **)&c->xin, (size_t)(Tm * H) * 2},
+      {(void **)&c->xout, (size_t)(Tm * H) * 2},
+      {(void **)&c->err, 16},
+  };
+  size_t total = 0;
+  for (auto &s : slots) total += align_up(s.bytes, 256);
+  if (cudaMalloc(&c->ws, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return MOE_ERR_NOMEM;
+  }
+  c->ws_bytes = total;
+  size_t off = 0;
+  for (auto &s : slots) {
+    *s.p = c->ws + off;
+    off += align_up(s.bytes, 256);
+  }
+  if (cudaMemset(c->ws, 0, total) != cudaSuccess) {
+    cudaFree(c->ws);
+    delete c;
+    return MOE_ERR_CUDA;
+  }
+  *out = c;
+  return MOE_OK;
+}
+
+void moe_free(moe_ctx *c) {
+  if (c == nullptr) return;
+  cudaSetDevice(c->cfg.device);
+  drain_timing(c);
+  for (auto e : c->spare) cudaEventDestroy(e);
+  if (c->ws) cudaFree(c->ws);
+  delete c;
+}
+
+int moe_layer_forward(moe_ctx *c, const void *hidden, int64_t T, const float *rw,
+                      const float *rb, const uint8_t *w13, const float *s13, const uint8_t *w2,
+                      const float *s2, int32_t top_k, void *out, void *stream) {
+  int rc = check_forward_args(c, hidden, T, rw, rb, w13, s13, w2, s2, top_k, out);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) {
+    c->last_T = 0;
+    c->last_k = top_k;
+    return MOE_OK;
+  }
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  return forward_device(c, (const __nv_bfloat16 *)hidden, T, rw, rb, w13, s13, w2, s2, top_k,
+                        (__nv_bfloat16 *)out, (cudaStream_t)stream);
+}
+
+int moe_layer_forward_host(moe_ctx *c, const void *hidden_host, int64_t T, const float *rw,
+                           const float *rb, const uint8_t *w13, const float *s13,
+                           const uint8_t *w2, const float *s2, int32_t top_k, void *out_host,
+                           void *stream) {
+  if (c == nullptr) return MOE_ERR_ARG;
+  int rc = check_forward_args(c, c->xin, T, rw, rb, w13, s13, w2, s2, top_k, c->xout);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) return MOE_OK;
+  if (!hidden_host || !out_host) return MOE_ERR_ARG;
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t bytes = (size_t)(T * c->cfg.hidden) * 2;
+  CUDA_TRY(cudaMemcpyAsync(c->xin, hidden_host, bytes, cudaMemcpyHostToDevice, s));
+  rc = forward_device(c, c->xin, T, rw, rb, w13, s13, w2, s2, top_k, c->xout, s);
+  if (rc != MOE_OK) return rc;
+  CUDA_TRY(cudaMemcpyAsync(out_host, c->xout, bytes, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return MOE_OK;
+}
+
+int moe_get_routing(moe_ctx *c, int32_t *idx, float *wts, int32_t *counts, int32_t *offsets,
+                    int32_t *perm, int32_t *inv, void *stream) {
+  if (c == nullptr) return MOE_ERR_ARG;
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t P = (size_t)(c->last_T * c->last_k), E = (size_t)c->cfg.n_experts;
+  const cudaMemcpyKind d2d = cudaMemcpyDeviceToDevice;
+  if (idx && P) CUDA_TRY(cudaMemcpyAsync(idx, c->idx, P * 4, d2d, s));
+  if (wts && P) CUDA_TRY(cudaMemcpyAsync(wts, c->wts, P * 4, d2d, s));
+  if (counts) CUDA_TRY(cudaMemcpyAsync(counts, c->counts, E * 4, d2d, s));
+  if (offsets) CUDA_TRY(cudaMemcpyAsync(offsets, c->offsets, (E + 1) * 4, d2d, s));
+  if (perm && P) CUDA_TRY(cudaMemcpyAsync(perm, c->perm, P * 4, d2d, s));
+  if (inv && P) CUDA_TRY(cudaMemcpyAsync(inv, c->inv, P * 4, d2d, s));
+  return MOE_OK;
+}
+
+int moe_status(moe_ctx *c) {
+  if (c == nullptr) return MOE_ERR_ARG;
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(c->last_stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int flag = 0;
+  CUDA_TRY(cudaMemcpy(&flag, c->err, sizeof(int), cudaMemcpyDeviceToHost));
+  CUDA_TRY(cudaMemset(c->err, 0, sizeof(int)));
+  if (flag & DEV_ERR_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
+  if (flag & DEV_ERR_NONFINITE) return MOE_ERR_NONFINITE;
+  if (flag) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+int moe_set_path(moe_ctx *c, int path) {
+  if (c == nullptr) return MOE_ERR_ARG;
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GEMM) return MOE_ERR_ARG;
+  c->path = path;
+  return MOE_OK;
+}
+
+int moe_set_timing(moe_ctx *c, int mask) {
+  if (c == nullptr) return MOE_ERR_ARG;
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  drain_timing(c);
+  for (int k = 0; k < MOE_K_COUNT; ++k) {
+    c->total_ms[k] = 0.0;
+    c->launches[k] = 0;
+  }
+  c->timing = mask & ((1 << MOE_K_COUNT) - 1);
+  return MOE_OK;
+}
+
+int64_t moe_launch_count(moe_ctx *c) { return c ? c->n_launches : -1; }
+
+int moe_kernel_time(moe_ctx *c, int kernel, double *total_ms, int64_t *launches) {
+  if (c == nullptr || kernel < 0 || kernel >= MOE_K_COUNT) return MOE_ERR_ARG;
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  drain_timing(c);
+  if (total_ms) *total_ms = c->total_ms[kernel];
+  if (launches) *launches = c->launches[kernel];
+  return MOE_OK;
+}
+
+int moe_debug_copy(moe_ctx *c, const char *name, void *dst, int64_t capacity, int64_t *nbytes,
+                   void *stream) {
+  if (c == nullptr || name == nullptr || capacity < 0) return MOE_ERR_ARG;
+  const int64_t T = c->last_T, P = c->last_T * c->last_k;
+  const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, I = c->cfg.inter;
+  const void *p = nullptr;
+  int64_t n = 0;
+  if (!strcmp(name, "logits")) { p = c->logits; n = T * E * 4; }
+  else if (!strcmp(name, "h")) { p = c->h; n = P * I * 4; }
+  else if (!strcmp(name, "y")) { p = c->y; n = P * H * 4; }
+  else if (!strcmp(name, "x16")) { p = c->x16; n = T * H * 2; }
+  else return MOE_ERR_ARG;
+  if (nbytes) *nbytes = n;
+  const int64_t m = n < capacity ? n : capacity;
+  if (m > 0) {
+    if (dst == nullptr) return MOE_ERR_ARG;
+    if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+    CUDA_TRY(cudaMemcpyAsync(dst, p, (size_t)m, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+  }
+  return MOE_OK;
+}
+
+}  // extern "C"

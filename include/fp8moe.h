@@ -1,0 +1,190 @@
+/*
+ * fp8moe.h - C ABI of a GB300 (sm_103a) routed Mixture-of-Experts FFN layer
+ * whose expert weights are blockwise FP8.
+ *
+ * The layer (one decoder MoE block's routed experts) computes, for T tokens:
+ *   1. router logits in f32 inputs (dragon.c, "Precision": router f32),
+ *      top-k by logit with ties to the lower expert index (Trochilus, "What
+ *      makes it different", the lowest row wins a tie), weights = softmax over
+ *      the k selected logits (softmax, top-k, renormalise);
+ *   2. a histogram / exclusive scan / stable scatter of the T*k (token,
+ *      expert) pairs by expert (Trochilus, "Acknowledgements": pairs sorted by
+ *      a counting sort);
+ *   3. per expert, SwiGLU: h = silu(W13[e, :I] x) * (W13[e, I:] x), with the
+ *      gate rows before the up rows (DeepSeek-V4.1-Flash post, "Repack experts
+ *      for the disk": gate | up | down);
+ *   4. y = W2[e] h;
+ *   5. out[t] = bf16( sum over r = 0..k-1, in router rank order, of
+ *      w[t, r] * y[t, r] ) (WARP BACKENDS.md, "Coherent memory": partials
+ *      reduced in original router order), with no float atomics.
+ * Weights are e4m3 codes with one f32 scale per 128x128 block, stored with
+ * the weights (dragon.c, "Precision"); a weight's value is its code's value
+ * times its block's scale.
+ *
+ * Conventions (every call):
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code; nothing throws.
+ *   - Tensor arguments are raw pointers; "device" pointers must be CUDA
+ *     device (or managed) memory of the context's device.  The caller owns
+ *     every tensor; the context owns only its workspace.
+ *   - All integer sizes are int64_t; all index arithmetic inside is 64-bit.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the host is not synchronised, except where stated.
+ *   - One context serves one stream at a time: calls on one context must not
+ *     overlap on the GPU.
+ */
+#ifndef FP8MOE_H
+#define FP8MOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_OK 0
+#define MOE_ERR_ARG (-1)            /* NULL pointer, bad enum, T < 0          */
+#define MOE_ERR_SHAPE (-2)          /* H or I not a multiple of 128, k out of  */
+                                    /* [1, min(E, max_top_k)], T > max_tokens  */
+#define MOE_ERR_ALIGN (-3)          /* a pointer breaks its stated alignment   */
+#define MOE_ERR_CUDA (-4)           /* a CUDA runtime/driver call failed       */
+#define MOE_ERR_DEVICE_TIMEOUT (-5) /* a bounded device-side wait gave up      */
+#define MOE_ERR_NOMEM (-6)          /* workspace allocation failed             */
+#define MOE_ERR_UNSUPPORTED (-7)    /* device is not compute capability 10.3   */
+#define MOE_ERR_NONFINITE (-8)      /* a router logit was NaN or infinite      */
+#define MOE_ERR_DEVICE (-9)         /* a device-side consistency check failed  */
+
+typedef struct moe_ctx moe_ctx; /* opaque; owned by the library */
+
+typedef struct moe_config {
+  int64_t max_tokens; /* largest T a forward may be called with (> 0)            */
+  int64_t hidden;     /* H: model width, multiple of 128, <= 65536              */
+  int64_t n_experts;  /* E: routed experts, 1..1024                             */
+  int64_t inter;      /* I: expert FFN width, multiple of 128, <= 65536         */
+  int32_t max_top_k;  /* largest k a forward may use, 1..min(E, 32)             */
+  int32_t device;     /* CUDA device ordinal the context lives on              */
+} moe_config;
+
+/*
+ * moe_init - validate `cfg` and allocate a context with a device workspace
+ * sized for max_tokens * max_top_k (token, expert) pairs.
+ *   out : receives the new context (host pointer to a host pointer).
+ * Errors: MOE_ERR_ARG (NULL), MOE_ERR_SHAPE (cfg out of range; checked before
+ * any CUDA call), MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_NOMEM.  On error
+ * *out is set to NULL and nothing is leaked.
+ */
+int moe_init(moe_ctx **out, const moe_config *cfg);
+
+/*
+ * moe_layer_forward - run the layer on T tokens (steps 1-5 above).
+ *   hidden      : device, bf16 [T, H] row-major, 16-byte aligned.
+ *   router_w    : device, f32 [E, H] row-major, 16-byte aligned.
+ *   router_bias : device, f32 [E], or NULL for none.  When present it is added
+ *                 to the logits before selection and softmax.
+ *   w13         : device, e4m3 [E, 2I, H] row-major (rows [0,I) gate,
+ *                 [I,2I) up), 16-byte aligned.
+ *   s13         : device, f32 [E, 2I/128, H/128] block scales, 4-byte aligned.
+ *   w2          : device, e4m3 [E, H, I] row-major, 16-byte aligned.
+ *   s2          : device, f32 [E, H/128, I/128] block scales, 4-byte aligned.
+ *   top_k       : k, in [1, min(E, max_top_k)].
+ *   out         : device, bf16 [T, H], 16-byte aligned; must not overlap any
+ *                 input.
+ *   stream      : cudaStream_t or NULL.
+ * T = 0 is a no-op.  Routing is exact: indices, counts and the permutation
+ * equal those of exact arithmetic on the inputs (f32 logits carry a rigorous
+ * error bound; tokens whose order the bound cannot certify are recomputed
+ * in f64).  Device-side failures (a bounded wait that gave up, a non-finite
+ * logit) are recorded in the context and reported by moe_status.
+ */
+int moe_layer_forward(moe_ctx *ctx, const void *hidden, int64_t T, const float *router_w,
+                      const float *router_bias, const uint8_t *w13, const float *s13,
+                      const uint8_t *w2, const float *s2, int32_t top_k, void *out,
+                      void *stream);
+
+/*
+ * moe_layer_forward_host - moe_layer_forward with the activations in HOST
+ * memory: copies hidden_host (bf16 [T, H]) to the device, runs the layer, and
+ * copies the result into out_host (bf16 [T, H]).  Weights stay device
+ * pointers as in moe_layer_forward.  Host buffers should be pinned
+ * (cudaHostAlloc / cudaHostRegister) for asynchronous copies.  The call
+ * returns after the result is in out_host (it synchronises `stream`).
+ */
+int moe_layer_forward_host(moe_ctx *ctx, const void *hidden_host, int64_t T,
+                           const float *router_w, const float *router_bias, const uint8_t *w13,
+                           const float *s13, const uint8_t *w2, const float *s2, int32_t top_k,
+                           void *out_host, void *stream);
+
+/*
+ * moe_get_routing - copy the routing of the last forward into caller device
+ * buffers (any may be NULL to skip it).  Sizes for that forward's T and k,
+ * P = T*k:
+ *   idx     int32 [T, k]  experts of each token in rank order
+ *   wts     f32   [T, k]  renormalised weights, same order
+ *   counts  int32 [E]     pairs routed to each expert
+ *   offsets int32 [E+1]   exclusive scan of counts
+ *   perm    int32 [P]     position -> pair id p = t*k + r, ascending p within
+ *                         each expert segment
+ *   inv     int32 [P]     pair id -> position
+ * Enqueued on `stream`.
+ */
+int moe_get_routing(moe_ctx *ctx, int32_t *idx, float *wts, int32_t *counts, int32_t *offsets,
+                    int32_t *perm, int32_t *inv, void *stream);
+
+/*
+ * moe_status - synchronise the context's last stream and return MOE_OK or
+ * the first device-side error recorded since the previous call (the flag is
+ * cleared).
+ */
+int moe_status(moe_ctx *ctx);
+
+/* moe_free - release the context and its workspace; NULL is a no-op. */
+void moe_free(moe_ctx *ctx);
+
+/* moe_strerror - static description of a return code. */
+const char *moe_strerror(int code);
+
+/*
+ * Path selection.  MOE_PATH_AUTO picks the grouped-GEMV path for
+ * T <= 64 and the tensor-core grouped-GEMM path above; the other values force
+ * one path (both compute the same layer).
+ */
+#define MOE_PATH_AUTO 0
+#define MOE_PATH_GEMV 1
+#define MOE_PATH_GEMM 2
+int moe_set_path(moe_ctx *ctx, int path);
+
+/*
+ * Kernel timing.  moe_set_timing(ctx, mask) records CUDA events around each
+ * kernel whose bit (1 << MOE_K_*) is set in `mask`, on the forward's stream
+ * (mask 0 turns timing off; every call resets the totals).  moe_kernel_time
+ * returns the summed device time (ms) and the number of timed launches of one
+ * kernel (it synchronises).  moe_launch_count returns how many kernels the
+ * context has launched since moe_init, timed or not.
+ */
+#define MOE_K_ROUTER_LOGITS 0
+#define MOE_K_ROUTER_SELECT 1
+#define MOE_K_PERMUTE 2
+#define MOE_K_GATE_UP 3 /* grouped GEMV or GEMM for W13 with SwiGLU */
+#define MOE_K_DOWN 4    /* grouped GEMV or GEMM for W2            */
+#define MOE_K_COMBINE 5
+#define MOE_K_ACT_QUANT 6
+#define MOE_K_COUNT 7
+int moe_set_timing(moe_ctx *ctx, int mask);
+int moe_kernel_time(moe_ctx *ctx, int kernel, double *total_ms, int64_t *launches);
+int64_t moe_launch_count(moe_ctx *ctx);
+const char *moe_kernel_name(int kernel);
+
+/*
+ * moe_debug_copy - copy a workspace buffer of the last forward into a caller
+ * device buffer, for tests: "logits" f32 [T,E], "h" f32 [P,I] (GEMV path,
+ * position order), "y" f32 [P,H] (position order), "x16" f16 [T,H].  Copies
+ * min(capacity, size) bytes on `stream` and stores the buffer's full size in
+ * *nbytes (may be NULL).
+ */
+int moe_debug_copy(moe_ctx *ctx, const char *name, void *dst, int64_t capacity, int64_t *nbytes,
+                   void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8MOE_H */

@@ -1,0 +1,96 @@
+"""Shared helpers of the GPU parity tests: upload, run through the C ABI,
+compare with the oracle.
+
+Tolerances (the CUDA path against the f64 oracle):
+  * routing indices, counts, offsets, permutation, inverse: bit-exact;
+  * routing weights: |w_gpu - w_oracle| <= WTS_ATOL.  The weights of a
+    certified token come from f32 logits whose error is below the router's
+    bound (about 1e-5 relative to ||x|| ||W_e|| at the largest H here) and a
+    few f32 roundings of the softmax; typical errors are about 1e-7;
+  * bf16 outputs: relative L2 error <= 1e-2 and max |error| <= 2e-2 x RMS of
+    the oracle output, both against the unrounded f64 oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as W
+from fp8_routed_expert_gb300 import MoELayer
+
+REL_L2 = 1e-2
+MAXABS_RMS = 2e-2
+WTS_ATOL = 2e-5
+
+DEV = torch.device("cuda", 0)
+
+
+def dev(a: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+
+
+def x_dev(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).astype(np.int16)).view(torch.bfloat16).to(DEV)
+
+
+class DeviceWeights:
+    def __init__(self, w: W.LayerWeights):
+        self.host = w
+        self.router_w = dev(w.router_w)
+        self.router_bias = None if w.router_bias is None else dev(w.router_bias)
+        self.w13, self.s13 = dev(w.w13), dev(w.s13)
+        self.w2, self.s2 = dev(w.w2), dev(w.s2)
+
+    def args(self):
+        return (self.router_w, self.router_bias, self.w13, self.s13, self.w2, self.s2)
+
+
+def make_layer(fam: W.Family, max_tokens: int, max_top_k: int | None = None) -> MoELayer:
+    return MoELayer(max_tokens, fam.hidden, fam.n_experts, fam.inter, max_top_k or fam.top_k, 0)
+
+
+def run(layer: MoELayer, x_bits: np.ndarray, dw: DeviceWeights, k: int, path: str = "auto"):
+    """Forward through the C ABI; returns (out bf16 bits [T,H], routing dict of numpy)."""
+    layer.set_path(path)
+    xt = x_dev(x_bits)
+    out = layer.forward(xt, *dw.args(), k)
+    T = x_bits.shape[0]
+    r = layer.routing(T, k)
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    r = {name: t.cpu().numpy() for name, t in r.items()}
+    return out.view(torch.int16).cpu().numpy().astype(np.uint16), r
+
+
+def reference(x_bits, w: W.LayerWeights, k: int, tokens=None, keep_h=False):
+    return oracle.moe_forward(x_bits, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2, k,
+                              tokens=tokens, keep_h=keep_h)
+
+
+def output_errors(out_bits: np.ndarray, ref_out: np.ndarray):
+    got = oracle.bf16_to_f64(out_bits)
+    diff = got - ref_out
+    rms = np.sqrt(np.mean(ref_out ** 2))
+    rel = np.linalg.norm(diff) / max(np.linalg.norm(ref_out), 1e-300)
+    mx = np.abs(diff).max() / max(rms, 1e-300) if diff.size else 0.0
+    return rel, mx
+
+
+def check_routing(r: dict, ref: dict, n_experts: int):
+    assert np.array_equal(r["idx"], ref["idx"]), "routing indices differ"
+    assert np.array_equal(r["counts"], ref["counts"]), "counts differ"
+    assert np.array_equal(r["offsets"], ref["offsets"]), "offsets differ"
+    assert np.array_equal(r["perm"], ref["perm"]), "permutation differs"
+    assert np.array_equal(r["inv"], ref["inv"]), "inverse permutation differs"
+    err = np.abs(r["wts"].astype(np.float64) - ref["wts"]).max()
+    assert err <= WTS_ATOL, f"routing weights differ by {err:.2e}"
+    return err
+
+
+def check_output(out_bits: np.ndarray, ref: dict, tokens=None):
+    sel = ref["tokens"] if tokens is None else tokens
+    rel, mx = output_errors(out_bits[sel], ref["out"])
+    assert rel <= REL_L2, f"relative L2 error {rel:.3e} > {REL_L2}"
+    assert mx <= MAXABS_RMS, f"max abs error {mx:.3e} x RMS > {MAXABS_RMS}"
+    return rel, mx

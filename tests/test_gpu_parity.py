@@ -1,0 +1,267 @@
+"""CUDA path vs the f64 CPU oracle, through the C ABI (needs an sm_103a GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from fp8_routed_expert_gb300 import C, MoEError
+from harness import (DeviceWeights, check_output, check_routing, make_layer, reference, run,
+                     x_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+_weights = {}
+
+
+def weights(name):
+    if name not in _weights:
+        fam = W.family(name)
+        w = W.make_weights(fam)
+        _weights.clear()
+        torch.cuda.empty_cache()
+        _weights[name] = (fam, w, DeviceWeights(w))
+    return _weights[name]
+
+
+# ------------------------------------------------------------------ full parity
+
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+def test_tiny(path):
+    fam, w, dw = weights("tiny")
+    x = W.make_x(fam, 4)
+    layer = make_layer(fam, 4)
+    out, r = run(layer, x, dw, fam.top_k, path)
+    ref = reference(x, w, fam.top_k)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref)
+
+
+@pytest.mark.parametrize("T", [1, 8])
+@pytest.mark.parametrize("path", ["gemv", "gemm"])
+def test_olmoe_decode(T, path):
+    fam, w, dw = weights("olmoe_decode")
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, fam.top_k, path)
+    ref = reference(x, w, fam.top_k)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref)
+
+
+@pytest.mark.parametrize("T", [2, 17, 64, 65, 127, 129, 300])
+def test_olmoe_ragged_batches(T):
+    """Batches that straddle the GEMV/GEMM switch and the 128-row tiles."""
+    fam, w, dw = weights("olmoe_decode")
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, fam.top_k, "auto")
+    ref = reference(x, w, fam.top_k)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref)
+
+
+def test_intermediates_match_oracle():
+    """Per-kernel parity: h after gate/up + SwiGLU and y after the down GEMV."""
+    fam, w, dw = weights("olmoe_decode")
+    T, k = 8, fam.top_k
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    run(layer, x, dw, k, "gemv")
+    ref = reference(x, w, k, keep_h=True)
+    P = T * k
+    h = layer.debug_buffer("h", torch.float32, (P, fam.inter)).cpu().numpy().astype(np.float64)
+    y = layer.debug_buffer("y", torch.float32, (P, fam.hidden)).cpu().numpy().astype(np.float64)
+    perm = ref["perm"]
+    ref_h = ref["h"].reshape(P, fam.inter)[perm]
+    ref_y = ref["y"].reshape(P, fam.hidden)[perm]
+    assert np.linalg.norm(h - ref_h) / np.linalg.norm(ref_h) < 1e-4
+    assert np.linalg.norm(y - ref_y) / np.linalg.norm(ref_y) < 1e-4
+
+
+# ------------------------------------------------------------------ full-size workloads
+
+@pytest.mark.parametrize("T", [512, 2048])
+def test_olmoe_prefill(T):
+    fam, w, dw = weights("olmoe_prefill")
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, fam.top_k, "auto")
+    tokens = None if T <= 512 else np.r_[0:8, T // 2:T // 2 + 8, T - 8:T]
+    ref = reference(x, w, fam.top_k, tokens=tokens)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref, tokens)
+    assert (ref["counts"] > 0).all() and ref["counts"].max() > 2 * ref["counts"].mean()
+
+
+@pytest.mark.parametrize("T", [1, 16, 64])
+def test_wide_decode(T):
+    fam, w, dw = weights("wide_decode")
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, fam.top_k, "auto")
+    tokens = None if T <= 16 else np.r_[0:4, T - 4:T]
+    ref = reference(x, w, fam.top_k, tokens=tokens)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref, tokens)
+
+
+def test_large_prefill_sampled():
+    fam, w, dw = weights("large_prefill")
+    T = 4096
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, fam.top_k, "auto")
+    ref_r = reference(x, w, fam.top_k, tokens=[])
+    check_routing(r, ref_r, fam.n_experts)
+    counts = ref_r["counts"]
+    assert (counts == 0).any(), "the workload should leave some experts without tokens"
+    busiest = int(np.argmax(counts))
+    t_busy = int(ref_r["perm"][ref_r["offsets"][busiest]] // fam.top_k)
+    tokens = np.array(sorted({0, 1, t_busy, T // 2, T - 1}))
+    ref = reference(x, w, fam.top_k, tokens=tokens)
+    check_output(out, ref, tokens)
+
+
+# ------------------------------------------------------------------ degenerate cases
+
+def _tiny_layer(max_top_k=None, max_tokens=8):
+    fam, w, dw = weights("tiny")
+    return fam, w, dw, make_layer(fam, max_tokens, max_top_k)
+
+
+def test_identical_router_rows_tie_to_lower_index():
+    fam, w, dw, layer = _tiny_layer()
+    rw = w.router_w.copy()
+    rw[:] = rw[3]
+    w2 = W.LayerWeights(rw, None, w.w13, w.s13, w.w2, w.s2)
+    x = W.make_x(fam, 4)
+    out, r = run(layer, x, DeviceWeights(w2), fam.top_k)
+    assert (r["idx"] == np.arange(fam.top_k)).all()
+    assert np.allclose(r["wts"], 1.0 / fam.top_k, rtol=1e-7)
+    ref = reference(x, w2, fam.top_k)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref)
+
+
+def test_near_ties_are_resolved_exactly():
+    """Router rows that differ in one element by one ulp: f32 logits tie or
+    flip, the exact order is decided by the f64 recomputation."""
+    fam, w, dw, layer = _tiny_layer()
+    rw = w.router_w.copy()
+    for e in range(1, fam.n_experts):
+        rw[e] = rw[0]
+        rw[e, e] = np.nextafter(rw[0, e], np.float32(np.inf) if e % 2 else np.float32(-np.inf))
+    w2 = W.LayerWeights(rw, None, w.w13, w.s13, w.w2, w.s2)
+    x = W.make_x(fam, 4)
+    out, r = run(layer, x, DeviceWeights(w2), fam.top_k)
+    ref = reference(x, w2, fam.top_k)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref)
+
+
+def test_zero_input():
+    fam, w, dw, layer = _tiny_layer()
+    x = np.zeros((3, fam.hidden), dtype=np.uint16)
+    out, r = run(layer, x, dw, fam.top_k)
+    assert (out & 0x7FFF == 0).all()
+    assert (r["idx"] == np.arange(fam.top_k)).all()
+
+
+@pytest.mark.parametrize("k", [1, 8])
+def test_k_extremes(k):
+    fam, w, dw, layer = _tiny_layer(max_top_k=8)
+    x = W.make_x(fam, 4)
+    out, r = run(layer, x, dw, k)
+    ref = reference(x, w, k)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref)
+
+
+def test_large_activations_use_exact_power_of_two_scaling():
+    fam, w, dw, layer = _tiny_layer()
+    x = W.make_x(fam, 4)
+    big = (oracle.bf16_to_f64(x) * 2.0 ** 17).astype(np.float32)  # exact in bf16
+    xb = (big.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.abs(oracle.bf16_to_f64(xb)).max() > 65504
+    out, r = run(layer, xb, dw, fam.top_k)
+    ref = reference(xb, w, fam.top_k)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref)
+
+
+def test_T_equals_max_tokens_and_zero():
+    fam, w, dw, layer = _tiny_layer(max_tokens=5)
+    x = W.make_x(fam, 5)
+    out, r = run(layer, x, dw, fam.top_k)
+    check_output(out, reference(x, w, fam.top_k))
+    empty = torch.empty((0, fam.hidden), dtype=torch.bfloat16, device="cuda")
+    layer.forward(empty, *dw.args(), fam.top_k)
+    assert layer.status() == 0
+
+
+def test_deterministic_bytes():
+    fam, w, dw = weights("olmoe_decode")
+    x = W.make_x(fam, 8)
+    layer = make_layer(fam, 8)
+    a = run(layer, x, dw, fam.top_k)
+    b = run(layer, x, dw, fam.top_k)
+    assert np.array_equal(a[0], b[0])
+    for key in a[1]:
+        assert np.array_equal(a[1][key], b[1][key])
+
+
+def test_host_buffer_entry_point_matches():
+    fam, w, dw = weights("olmoe_decode")
+    T = 8
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out_dev, _ = run(layer, x, dw, fam.top_k)
+    xh = torch.from_numpy(x.astype(np.int16)).view(torch.bfloat16).pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    layer.forward_host(xh, *dw.args(), fam.top_k, oh)
+    assert np.array_equal(oh.view(torch.int16).numpy().astype(np.uint16), out_dev)
+
+
+def test_argument_errors():
+    fam, w, dw, layer = _tiny_layer(max_tokens=4)
+    x = x_dev(W.make_x(fam, 4))
+    with pytest.raises(MoEError) as e:
+        layer.forward(x, *dw.args(), 3)                  # k > max_top_k
+    assert e.value.code == C["MOE_ERR_SHAPE"]
+    x5 = x_dev(W.make_x(fam, 5))
+    with pytest.raises(MoEError) as e:
+        layer.forward(x5, *dw.args(), 2)                 # T > max_tokens
+    assert e.value.code == C["MOE_ERR_SHAPE"]
+    from fp8_routed_expert_gb300 import lib
+    buf = torch.empty(4 * fam.hidden + 8, dtype=torch.bfloat16, device="cuda")
+    a = dw.args()
+    rc = lib().moe_layer_forward(layer.handle, buf.data_ptr() + 2, 4, a[0].data_ptr(), None,
+                                 a[2].data_ptr(), a[3].data_ptr(), a[4].data_ptr(), a[5].data_ptr(),
+                                 2, buf.data_ptr(), None)
+    assert rc == C["MOE_ERR_ALIGN"]
+
+
+def test_kernel_timing_api():
+    fam, w, dw = weights("olmoe_decode")
+    x = W.make_x(fam, 8)
+    layer = make_layer(fam, 8)
+    layer.set_timing("all")
+    n0 = layer.launch_count()
+    for _ in range(3):
+        run(layer, x, dw, fam.top_k)
+    assert layer.launch_count() - n0 == 3 * 6
+    for name in ("router_logits", "router_select", "permute", "gate_up", "down", "combine"):
+        ms, n = layer.kernel_time(name)
+        assert n == 3 and ms > 0, name
+    layer.set_timing(["gate_up"])
+    run(layer, x, dw, fam.top_k)
+    assert layer.kernel_time("gate_up")[1] == 1 and layer.kernel_time("down")[1] == 0
+    layer.set_timing(())
