@@ -101,3 +101,40 @@ __device__ __forceinline__ int f16_range_shift(float m) {
 }
 
 }  // namespace fp8moe
+
+namespace fp8moe {
+
+// Exponent e of the power-of-two block scale 2^e for a block whose largest
+// magnitude is amax: the smallest e with amax / 2^e <= 448 (the largest e4m3
+// value), so scaling is exact and the block's values land in [-448, 448].
+// 0 for an all-zero block.
+__device__ __forceinline__ int e4m3_block_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  int q;
+  const float m = frexpf(amax / 448.f, &q);  // amax / 448 = m 2^q, m in [0.5, 1)
+  return m > 0.5f ? q : q - 1;
+}
+
+// Multi-term e4m3 encoding of values already divided by their power-of-two
+// block scale (|v| <= 448): v ~= t0 + t1 + ... with t0 = e4m3(v),
+// t1 = e4m3(v - t0), ..., each rounded to nearest even and saturated
+// (cvt.rn.satfinite).  Each term carries 4 significant bits, so two terms
+// hold a bf16 value exactly (down to 2^-10 of the block scale) and three
+// terms keep about 12 bits of an f32 value.  Codes of (v0, v1), first value
+// in the low byte, one 16-bit pair per term.
+template <int NT>
+__device__ __forceinline__ void e4m3_terms(float v0, float v1, uint32_t (&codes)[NT]) {
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
+    codes[t] = c;
+    if (t + 1 < NT) {
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+      v0 -= f.x;
+      v1 -= f.y;
+    }
+  }
+}
+
+}  // namespace fp8moe

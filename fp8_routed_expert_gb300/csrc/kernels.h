@@ -1,6 +1,7 @@
 // Internal launchers of the layer's kernels (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -39,6 +40,22 @@ cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, con
                          const int32_t *counts, const int32_t *offsets, const int32_t *active,
                          const int32_t *n_active, int64_t H, int64_t I, float *y,
                          int64_t max_items, int wide_tokens, int grid_cap, cudaStream_t s);
+bool encode_u8_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows);
+cudaError_t launch_act_quant(const __nv_bfloat16 *x, const int32_t *perm, int64_t P, int k,
+                             int64_t H, int64_t Pmax, uint8_t *a_hi, uint8_t *a_lo, float *a_scale,
+                             int sms, cudaStream_t s);
+// Tensor maps of one grouped GEMM: up to three activation terms and the weights.
+struct TmapSet {
+  CUtensorMap a[3];
+  CUtensorMap b;
+};
+// mode 1: gate/up + SwiGLU -> three-term e4m3 h (two activation terms in);
+// mode 2: down -> f32 y (three activation terms in).
+cudaError_t launch_grouped_gemm(int mode, const TmapSet &tm, const int32_t *offsets,
+                                const int32_t *tile_offsets, const float *a_scale,
+                                const float *w_scale, int E, int64_t H, int64_t I, int64_t Pmax,
+                                uint8_t *const h_terms[3], float *h_scale, float *y, int *err,
+                                int64_t max_items, int sms, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const int32_t *inv, const float *wts, int64_t T, int k,
                            int64_t H, __nv_bfloat16 *out, cudaStream_t s);
 

@@ -36,6 +36,10 @@ struct moe_ctx {
   uint32_t *hmax = nullptr;
   __half *x16 = nullptr;
   __nv_bfloat16 *xin = nullptr, *xout = nullptr;  // staging for the host-buffer entry point
+  uint8_t *a_hi = nullptr, *a_lo = nullptr, *h_t[3] = {nullptr, nullptr, nullptr};
+  float *a_scale = nullptr, *h_scale = nullptr;  // [K/128][Pmax]
+  TmapSet tm_gemm1, tm_gemm2;                    // activation terms (workspace) + last weights
+  const void *tm_w13_ptr = nullptr, *tm_w2_ptr = nullptr;  // weights the maps in .b describe
   int *err = nullptr;
   int path = MOE_PATH_AUTO;
   // last forward
@@ -130,9 +134,9 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
                    const float *rb, const uint8_t *w13, const float *s13, const uint8_t *w2,
                    const float *s2, int k, __nv_bfloat16 *out, cudaStream_t s) {
   const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, I = c->cfg.inter;
-  const int64_t P = T * k;
-  const int path = c->path != MOE_PATH_AUTO ? c->path : (T <= kGemvMaxT ? MOE_PATH_GEMV : MOE_PATH_GEMM);
-  const int wide = (path == MOE_PATH_GEMM || T > kGemvMaxT) ? 1 : 0;
+  const int64_t P = T * k, Pm = c->cfg.max_tokens * c->cfg.max_top_k;
+  int path = c->path != MOE_PATH_AUTO ? c->path : (T <= kGemvMaxT ? MOE_PATH_GEMV : MOE_PATH_GEMM);
+  if (path == MOE_PATH_GEMM && H % 256 != 0) path = MOE_PATH_GEMV;  // GEMM2 tiles are 256 wide
   const int64_t max_active = P < E ? P : E;
   {
     Timed tm(c, MOE_K_ROUTER_LOGITS, s);
@@ -140,24 +144,55 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
   }
   {
     Timed tm(c, MOE_K_ROUTER_SELECT, s);
-    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm,
-                                  router_gamma(T, H), c->idx, c->wts, c->x16, c->xscale, c->err, s));
+    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, router_gamma(T, H),
+                                  c->idx, c->wts, path == MOE_PATH_GEMV ? c->x16 : nullptr,
+                                  c->xscale, c->err, s));
   }
   {
     Timed tm(c, MOE_K_PERMUTE, s);
     CUDA_TRY(launch_permute(c->idx, P, (int)E, kTileM, c->counts, c->offsets, c->perm, c->inv,
-                            c->active, c->n_active, c->tile_offsets, c->hmax, c->err, s));
+                            c->active, c->n_active, c->tile_offsets,
+                            path == MOE_PATH_GEMV ? c->hmax : nullptr, c->err, s));
   }
-  {
-    Timed tm(c, MOE_K_GATE_UP, s);
-    CUDA_TRY(launch_gemv13(w13, s13, c->x16, c->xscale, c->counts, c->offsets, c->perm, c->active,
-                           c->n_active, k, H, I, c->h, c->hmax, max_active * (I / 32), wide,
-                           c->sms * 4, s));
-  }
-  {
-    Timed tm(c, MOE_K_DOWN, s);
-    CUDA_TRY(launch_gemv2(w2, s2, c->h, c->hmax, c->counts, c->offsets, c->active, c->n_active, H,
-                          I, c->y, max_active * (H / 64), wide, c->sms * 4, s));
+  if (path == MOE_PATH_GEMV) {
+    const int wide = T > kGemvMaxT ? 1 : 0;
+    {
+      Timed tm(c, MOE_K_GATE_UP, s);
+      CUDA_TRY(launch_gemv13(w13, s13, c->x16, c->xscale, c->counts, c->offsets, c->perm,
+                             c->active, c->n_active, k, H, I, c->h, c->hmax,
+                             max_active * (I / 32), wide, c->sms * 4, s));
+    }
+    {
+      Timed tm(c, MOE_K_DOWN, s);
+      CUDA_TRY(launch_gemv2(w2, s2, c->h, c->hmax, c->counts, c->offsets, c->active, c->n_active,
+                            H, I, c->y, max_active * (H / 64), wide, c->sms * 4, s));
+    }
+  } else {
+    if (c->tm_w13_ptr != w13) {
+      if (!encode_u8_tmap(&c->tm_gemm1.b, w13, H, E * 2 * I, 64)) return MOE_ERR_CUDA;
+      c->tm_w13_ptr = w13;
+    }
+    if (c->tm_w2_ptr != w2) {
+      if (!encode_u8_tmap(&c->tm_gemm2.b, w2, I, E * H, 64)) return MOE_ERR_CUDA;
+      c->tm_w2_ptr = w2;
+    }
+    const int64_t max_tiles = (P + kTileM - 1) / kTileM + max_active;
+    {
+      Timed tm(c, MOE_K_ACT_QUANT, s);
+      CUDA_TRY(launch_act_quant(x, c->perm, P, k, H, Pm, c->a_hi, c->a_lo, c->a_scale, c->sms, s));
+    }
+    {
+      Timed tm(c, MOE_K_GATE_UP, s);
+      CUDA_TRY(launch_grouped_gemm(1, c->tm_gemm1, c->offsets, c->tile_offsets, c->a_scale, s13,
+                                   (int)E, H, I, Pm, c->h_t, c->h_scale, nullptr, c->err,
+                                   max_tiles * (I / 128), c->sms, s));
+    }
+    {
+      Timed tm(c, MOE_K_DOWN, s);
+      CUDA_TRY(launch_grouped_gemm(2, c->tm_gemm2, c->offsets, c->tile_offsets, c->h_scale, s2,
+                                   (int)E, H, I, Pm, nullptr, nullptr, c->y, c->err,
+                                   max_tiles * (H / 256), c->sms, s));
+    }
   }
   {
     Timed tm(c, MOE_K_COMBINE, s);
@@ -233,6 +268,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
 
   const int64_t Tm = cfg->max_tokens, E = cfg->n_experts, H = cfg->hidden, I = cfg->inter;
   const int64_t Pm = Tm * cfg->max_top_k;
+  const int64_t Pr = (Pm + 127) / 128 * 128;  // rows of the GEMM operand buffers (whole 128-row boxes)
   struct Slot {
     void **p;
     size_t bytes;
@@ -256,6 +292,13 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->xin, (size_t)(Tm * H) * 2},
       {(void **)&c->xout, (size_t)(Tm * H) * 2},
       {(void **)&c->err, 16},
+      {(void **)&c->a_hi, (size_t)(Pr * H)},
+      {(void **)&c->a_lo, (size_t)(Pr * H)},
+      {(void **)&c->a_scale, (size_t)(H / 128 * Pm) * 4},
+      {(void **)&c->h_t[0], (size_t)(Pr * I)},
+      {(void **)&c->h_t[1], (size_t)(Pr * I)},
+      {(void **)&c->h_t[2], (size_t)(Pr * I)},
+      {(void **)&c->h_scale, (size_t)(I / 128 * Pm) * 4},
   };
   size_t total = 0;
   for (auto &s : slots) total += align_up(s.bytes, 256);
@@ -271,6 +314,16 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
     off += align_up(s.bytes, 256);
   }
   if (cudaMemset(c->ws, 0, total) != cudaSuccess) {
+    cudaFree(c->ws);
+    delete c;
+    return MOE_ERR_CUDA;
+  }
+  if (!encode_u8_tmap(&c->tm_gemm1.a[0], c->a_hi, H, Pr, 128) ||
+      !encode_u8_tmap(&c->tm_gemm1.a[1], c->a_lo, H, Pr, 128) ||
+      !encode_u8_tmap(&c->tm_gemm1.a[2], c->a_lo, H, Pr, 128) ||
+      !encode_u8_tmap(&c->tm_gemm2.a[0], c->h_t[0], I, Pr, 128) ||
+      !encode_u8_tmap(&c->tm_gemm2.a[1], c->h_t[1], I, Pr, 128) ||
+      !encode_u8_tmap(&c->tm_gemm2.a[2], c->h_t[2], I, Pr, 128)) {
     cudaFree(c->ws);
     delete c;
     return MOE_ERR_CUDA;

@@ -23,20 +23,25 @@
 namespace fp8moe {
 
 // ------------------------------------------------------------------ logits, T small
-// One warp per expert row.  Lane l owns columns h = 128 j + 4 l .. +3; it sums
-// its 4 H/128 products sequentially with fma, then a 5-level butterfly adds
-// the 32 lane sums.  Rounding chain length: H/32 + 5 (+1 for the bias, added
-// in the select kernel).  Also writes ||W_e||_2.
+// One CTA of 8 warps per expert row; warp w owns the column slice
+// [w H/8, (w+1) H/8) and lane l the 4 columns 4 l + 128 j of that slice.  A
+// lane sums its products sequentially with fma, a 5-level butterfly adds the
+// 32 lanes, and one thread adds the 8 warp sums in order.  Rounding chain
+// length: 4 ceil(H/1024) + 5 + 8 (+1 for the bias, added in the select
+// kernel).  Also writes ||W_e||_2.
 template <int TG>
-__global__ void __launch_bounds__(128) router_logits_warp_kernel(
+__global__ void __launch_bounds__(256) router_logits_split_kernel(
     const __nv_bfloat16 *__restrict__ x, int64_t T, const float *__restrict__ W, int64_t E,
     int64_t H, float *__restrict__ logits, float *__restrict__ wnorm) {
-  const int lane = threadIdx.x & 31;
-  const int64_t e = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (e >= E) return;
+  __shared__ float part[8][TG];
+  __shared__ float ssq[8];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t e = blockIdx.x;
+  const int64_t slice = H / 8;
+  const int64_t h_lo = wid * slice, h_hi = h_lo + slice;
   const float *w = W + e * H;
   float ss = 0.f;
-  for (int64_t h = 4 * lane; h < H; h += 128) {
+  for (int64_t h = h_lo + 4 * lane; h < h_hi; h += 128) {
     float4 wv = __ldg(reinterpret_cast<const float4 *>(w + h));
     ss = fmaf(wv.x, wv.x, ss);
     ss = fmaf(wv.y, wv.y, ss);
@@ -44,18 +49,18 @@ __global__ void __launch_bounds__(128) router_logits_warp_kernel(
     ss = fmaf(wv.w, wv.w, ss);
   }
   ss = warp_sum(ss);
-  if (lane == 0) wnorm[e] = sqrtf(ss);
+  if (lane == 0) ssq[wid] = ss;
 
   for (int64_t t0 = 0; t0 < T; t0 += TG) {
     float acc[TG];
 #pragma unroll
     for (int j = 0; j < TG; ++j) acc[j] = 0.f;
-    for (int64_t h = 4 * lane; h < H; h += 128) {
-      float4 wv = __ldg(reinterpret_cast<const float4 *>(w + h));
+    for (int64_t h = h_lo + 4 * lane; h < h_hi; h += 128) {
+      const float4 wv = __ldg(reinterpret_cast<const float4 *>(w + h));
 #pragma unroll
       for (int j = 0; j < TG; ++j) {
         if (t0 + j < T) {
-          uint2 xv = __ldg(reinterpret_cast<const uint2 *>(x + (t0 + j) * H + h));
+          const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(x + (t0 + j) * H + h));
           acc[j] = fmaf(bf16_bits_to_float(xv.x & 0xffffu), wv.x, acc[j]);
           acc[j] = fmaf(bf16_bits_to_float(xv.x >> 16), wv.y, acc[j]);
           acc[j] = fmaf(bf16_bits_to_float(xv.y & 0xffffu), wv.z, acc[j]);
@@ -65,9 +70,23 @@ __global__ void __launch_bounds__(128) router_logits_warp_kernel(
     }
 #pragma unroll
     for (int j = 0; j < TG; ++j) {
-      float s = warp_sum(acc[j]);
-      if (lane == 0 && t0 + j < T) logits[(t0 + j) * E + e] = s;
+      const float s = warp_sum(acc[j]);
+      if (lane == 0) part[wid][j] = s;
     }
+    __syncthreads();
+    if (threadIdx.x < TG && t0 + threadIdx.x < T) {
+      float v = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v += part[q][threadIdx.x];
+      logits[(t0 + threadIdx.x) * E + e] = v;
+    }
+    if (t0 == 0 && threadIdx.x == 32) {
+      float v = 0.f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v += ssq[q];
+      wnorm[e] = sqrtf(v);
+    }
+    __syncthreads();
   }
 }
 
@@ -360,18 +379,16 @@ __global__ void __launch_bounds__(128) router_select_kernel(
 // ------------------------------------------------------------------ launchers
 
 int router_chain_depth(int64_t T, int64_t H) {
-  return T <= kRouterWarpMaxT ? (int)(H / 32 + 5 + 1) : (int)(128 + H / 128 + 1);
+  return T <= kRouterWarpMaxT ? (int)(4 * ((H + 1023) / 1024) + 5 + 8 + 1) : (int)(128 + H / 128 + 1);
 }
 
 cudaError_t launch_router_logits(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
                                  int64_t H, float *logits, float *wnorm, cudaStream_t s) {
   if (T <= kRouterWarpMaxT) {
-    const int warps = 4;
-    dim3 grid((unsigned)((E + warps - 1) / warps));
     if (T <= 1)
-      router_logits_warp_kernel<1><<<grid, 32 * warps, 0, s>>>(x, T, W, E, H, logits, wnorm);
+      router_logits_split_kernel<1><<<(unsigned)E, 256, 0, s>>>(x, T, W, E, H, logits, wnorm);
     else
-      router_logits_warp_kernel<8><<<grid, 32 * warps, 0, s>>>(x, T, W, E, H, logits, wnorm);
+      router_logits_split_kernel<8><<<(unsigned)E, 256, 0, s>>>(x, T, W, E, H, logits, wnorm);
     return cudaGetLastError();
   }
   row_norm_kernel<<<(unsigned)((E + 3) / 4), 128, 0, s>>>(W, E, H, wnorm);

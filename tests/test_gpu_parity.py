@@ -86,6 +86,27 @@ def test_intermediates_match_oracle():
     assert np.linalg.norm(y - ref_y) / np.linalg.norm(ref_y) < 1e-4
 
 
+@pytest.mark.parametrize("T", [16, 300])
+def test_gemm_path_y_matches_oracle(T):
+    """Per-kernel parity of the tensor-core path: y after the down GEMM
+    (position order) against the oracle's per-pair y.  Two e4m3 terms hold
+    the bf16 x exactly and three keep about 12 bits of h, so y stays near
+    1e-5 relative."""
+    fam, w, dw = weights("olmoe_decode")
+    k = fam.top_k
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, k, "gemm")
+    ref = reference(x, w, k)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref)
+    P = T * k
+    y = layer.debug_buffer("y", torch.float32, (P, fam.hidden)).cpu().numpy().astype(np.float64)
+    ref_y = ref["y"].reshape(P, fam.hidden)[ref["perm"]]
+    rel = np.linalg.norm(y - ref_y) / np.linalg.norm(ref_y)
+    assert rel < 2e-4, rel
+
+
 # ------------------------------------------------------------------ full-size workloads
 
 @pytest.mark.parametrize("T", [512, 2048])
