@@ -25,211 +25,335 @@
 
 namespace fp8moe {
 
-// ---------------------------------------------------------------- W13 + SwiGLU
-// Item = (active expert, 32 consecutive h outputs).  Warp w handles h rows
-// i0 = 8 (w % 4) .. +7 of the item: MMA rows 0..7 are gate rows i0.., rows
-// 8..15 the matching up rows I + i0.., so each lane ends with gate and up of
-// the same (h row, token) and applies SwiGLU itself.  Warps 0-3 take the first
-// half of the K blocks, warps 4-7 the second; the halves are added in shared
-// memory in a fixed order.
-template <int NT>
-__global__ void __launch_bounds__(256) gemv13_swiglu_kernel(
-    const uint8_t *__restrict__ w13, const float *__restrict__ s13, const __half *__restrict__ x16,
-    const float *__restrict__ xscale, const int32_t *__restrict__ counts,
-    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
-    const int32_t *__restrict__ active, const int32_t *__restrict__ n_active, int k, int64_t H,
-    int64_t I, float *__restrict__ h, uint32_t *__restrict__ hmax) {
-  __shared__ float red[4][32][NT][4];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int g = lane >> 2, q = lane & 3;
-  const int tile = wid & 3, half = wid >> 2;
-  const int64_t nkb = H / 128;
-  const int64_t kb_mid = (nkb + 1) / 2;
-  const int64_t kb_begin = half ? kb_mid : 0, kb_end = half ? nkb : kb_mid;
-  const int64_t items_per_expert = I / 32;
-  const int64_t n_items = (int64_t)(*n_active) * items_per_expert;
-  const int64_t srow = 2 * I / 128;
+// ---------------------------------------------------------------- staging
+// Each warp owns a contiguous range of items (16 weight rows x all of K) and
+// streams the rows through a private ring of shared-memory stages with 16-byte
+// cp.async copies (L2 only).  A stage holds two 128-wide K blocks of the 16
+// rows (4 KiB); copy instruction m moves 2 rows x 256 contiguous bytes, so
+// HBM sees row-sequential 256-byte runs.  In shared memory a stage is
+// [K block][row][128 bytes] with the 16-byte chunk index XORed by 4 (row & 1),
+// which keeps the MMA fragment reads (8 lanes = 2 rows per phase) free of bank
+// conflicts.  kRing - 1 stages (8 KiB per warp, 16 warps per SM) stay in
+// flight without holding registers; the ring runs across item boundaries.
 
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int e = active[item / items_per_expert];
-    const int64_t i0 = (item % items_per_expert) * 32 + tile * 8;
-    const int64_t cnt = counts[e], seg = offsets[e];
-    const uint8_t *wg_row = w13 + ((int64_t)e * 2 * I + i0 + g) * H + q * 16;
-    const uint8_t *wu_row = w13 + ((int64_t)e * 2 * I + I + i0 + g) * H + q * 16;
-    const float *sg = s13 + ((int64_t)e * srow + i0 / 128) * nkb;
-    const float *su = s13 + ((int64_t)e * srow + (I + i0) / 128) * nkb;
+constexpr int kStageKB = 2;                          // 128-wide K blocks per stage
+constexpr int kStageBytes = kStageKB * 16 * 128;    // 16 rows
+constexpr int kRing = 3;
+constexpr int kGemvWarps = 4;
 
-    for (int64_t tb = 0; tb < cnt; tb += NT * 8) {
-      const __half *xrow[NT];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const int64_t ti = tb + j * 8 + g;
-        xrow[j] = (ti < cnt) ? x16 + (int64_t)(perm[seg + ti] / k) * H + q * 16 : nullptr;
-      }
-      float tot[NT][4];
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int v = 0; v < 4; ++v) tot[j][v] = 0.f;
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
-      uint4 cg0, cg1, cu0, cu1;
-      if (kb_begin < kb_end) {
-        cg0 = ld_stream16(wg_row + kb_begin * 128);
-        cg1 = ld_stream16(wg_row + kb_begin * 128 + 64);
-        cu0 = ld_stream16(wu_row + kb_begin * 128);
-        cu1 = ld_stream16(wu_row + kb_begin * 128 + 64);
-      }
-      for (int64_t kb = kb_begin; kb < kb_end; ++kb) {
-        uint4 ng0, ng1, nu0, nu1;
-        if (kb + 1 < kb_end) {
-          ng0 = ld_stream16(wg_row + (kb + 1) * 128);
-          ng1 = ld_stream16(wg_row + (kb + 1) * 128 + 64);
-          nu0 = ld_stream16(wu_row + (kb + 1) * 128);
-          nu1 = ld_stream16(wu_row + (kb + 1) * 128 + 64);
-        }
-        float acc[NT][4];
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) acc[j][v] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint4 wg = c ? cg1 : cg0, wu = c ? cu1 : cu0;
-          uint4 xf[NT][2];
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            if (xrow[j] != nullptr) {
-              xf[j][0] = ld_ro16(xrow[j] + kb * 128 + c * 64);
-              xf[j][1] = ld_ro16(xrow[j] + kb * 128 + c * 64 + 8);
-            } else {
-              xf[j][0] = make_uint4(0, 0, 0, 0);
-              xf[j][1] = make_uint4(0, 0, 0, 0);
-            }
-          }
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint32_t gw = u4_word(wg, s), uw = u4_word(wu, s);
-            const uint32_t a0 = e4m3x2_to_f16x2(gw & 0xffffu);
-            const uint32_t a1 = e4m3x2_to_f16x2(uw & 0xffffu);
-            const uint32_t a2 = e4m3x2_to_f16x2(gw >> 16);
-            const uint32_t a3 = e4m3x2_to_f16x2(uw >> 16);
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-              mma_16816(acc[j], a0, a1, a2, a3, u4_word(xf[j][s >> 1], (2 * s) & 3),
-                        u4_word(xf[j][s >> 1], (2 * s + 1) & 3));
-          }
-        }
-        const float scg = __ldg(sg + kb), scu = __ldg(su + kb);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          tot[j][0] = fmaf(acc[j][0], scg, tot[j][0]);
-          tot[j][1] = fmaf(acc[j][1], scg, tot[j][1]);
-          tot[j][2] = fmaf(acc[j][2], scu, tot[j][2]);
-          tot[j][3] = fmaf(acc[j][3], scu, tot[j][3]);
-        }
-        cg0 = ng0; cg1 = ng1; cu0 = nu0; cu1 = nu1;
-      }
+// byte offset of (K block kbl, row, 16-byte chunk) inside a stage
+__device__ __forceinline__ int stage_off(int kbl, int row, int chunk) {
+  return kbl * 2048 + row * 128 + ((chunk ^ ((row & 1) << 2)) << 4);
+}
 
-      if (half == 1) {
+// Item range [lo, hi) of this warp: warps split the items into contiguous,
+// equal (+-1) ranges.
+__device__ __forceinline__ void warp_items(int n_items, int *lo, int *hi) {
+  const int64_t tw = (int64_t)gridDim.x * kGemvWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
+  *lo = (int)((int64_t)n_items * gw / tw);
+  *hi = (int)((int64_t)n_items * (gw + 1) / tw);
+}
+
+// Per-lane constants of the copy pattern: copy m (0..7) of a stage moves row
+// 2m + (lane >> 4), 16-byte chunk (lane & 15) of the stage's 256 bytes.
+struct CopyLane {
+  int soff;  // shared-memory byte offset of copy 0 (copy m adds 256 m)
+  int col;   // 16-byte chunk index 0..15 within the row's 256 bytes
+  int rpar;  // row parity (lane >> 4)
+};
+__device__ __forceinline__ CopyLane copy_lane(int lane) {
+  CopyLane c;
+  c.col = lane & 15;
+  c.rpar = lane >> 4;
+  c.soff = stage_off(c.col >> 3, c.rpar, c.col & 7);
+  return c;
+}
+
+// Converts the staged codes of one K block of rows g and g + 8 (fragment
+// offsets f0, f1 for the two 64-byte halves) to the f16 A registers of the
+// 8 k-steps: a[c][s][r].
+__device__ __forceinline__ void stage_fragments(const uint8_t *sk, int f0, int f1,
+                                                uint32_t (&a)[2][4][4]) {
+  const uint4 r0 = *reinterpret_cast<const uint4 *>(sk + f0);
+  const uint4 r1 = *reinterpret_cast<const uint4 *>(sk + f1);
+  const uint4 s0 = *reinterpret_cast<const uint4 *>(sk + f0 + 1024);
+  const uint4 s1 = *reinterpret_cast<const uint4 *>(sk + f1 + 1024);
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
+  for (int c = 0; c < 2; ++c) {
+    const uint4 lo = c ? r1 : r0, hi = c ? s1 : s0;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) red[tile][lane][j][v] = tot[j][v];
-      }
-      __syncthreads();
-      if (half == 0) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-#pragma unroll
-          for (int d = 0; d < 2; ++d) {
-            const int64_t ti = tb + j * 8 + 2 * q + d;
-            if (ti >= cnt) continue;
-            const int64_t pos = seg + ti;
-            const float xs = xscale[perm[pos] / k];
-            const float gv = (tot[j][d] + red[tile][lane][j][d]) * xs;
-            const float uv = (tot[j][2 + d] + red[tile][lane][j][2 + d]) * xs;
-            const float hv = swiglu(gv, uv);
-            h[pos * I + i0 + g] = hv;
-            atomicMax(&hmax[pos], __float_as_uint(fabsf(hv)));
-          }
-        }
-      }
-      __syncthreads();
+    for (int s4 = 0; s4 < 4; ++s4) {
+      const uint32_t lw = u4_word(lo, s4), hw = u4_word(hi, s4);
+      a[c][s4][0] = e4m3x2_to_f16x2(lw & 0xffffu);
+      a[c][s4][1] = e4m3x2_to_f16x2(hw & 0xffffu);
+      a[c][s4][2] = e4m3x2_to_f16x2(lw >> 16);
+      a[c][s4][3] = e4m3x2_to_f16x2(hw >> 16);
     }
   }
 }
 
-// ---------------------------------------------------------------- W2
-// Item = (active expert, 64 consecutive output rows).  Warp w computes rows
-// j0 = 16 (w % 4) .. +15 over one half of the K blocks of I.  The activations
-// h (f32) are split into an f16 pair hi + lo after an exact power-of-two
-// scaling chosen from the position's largest |h|, so the products keep about
-// 22 bits of h.
+// ---------------------------------------------------------------- W13 + SwiGLU
+// Item = (active expert, 8 consecutive h outputs i0..i0+7), one warp, all of
+// K.  MMA rows 0..7 are the gate rows i0.., rows 8..15 the matching up rows
+// I + i0.., so each lane ends with gate and up of the same (h row, token) and
+// applies SwiGLU itself.  Columns are up to 8 tokens of the expert per MMA;
+// NT groups of 8 share each staged weight chunk.
 template <int NT>
-__global__ void __launch_bounds__(256) gemv2_kernel(
+__global__ void __launch_bounds__(32 * kGemvWarps) gemv13_swiglu_kernel(
+    const uint8_t *__restrict__ w13, const float *__restrict__ s13, const __half *__restrict__ x16,
+    const float *__restrict__ xscale, const int32_t *__restrict__ counts,
+    const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
+    const int32_t *__restrict__ active, const int32_t *__restrict__ n_active, int k, int64_t H,
+    int64_t I, int64_t tb0, float *__restrict__ h, uint32_t *__restrict__ hmax) {
+  extern __shared__ __align__(128) uint8_t ring_all[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  uint8_t *ring = ring_all + wid * (kRing * kStageBytes);
+  const int ipe = (int)(I / 8);
+  const int nkb = (int)(H / 128);
+  const int nst = (nkb + kStageKB - 1) / kStageKB;
+  const int srow = (int)(2 * I / 128);
+  int it_lo, it_hi;
+  warp_items(*n_active * ipe, &it_lo, &it_hi);
+  if (it_lo >= it_hi) return;
+
+  // ---- producer cursor (stage being copied next)
+  const CopyLane cl = copy_lane(lane);
+  int is_item = it_lo, is_st = 0, is_slot = 0;
+  const uint8_t *is_gate = nullptr;
+  auto issue_item = [&]() {
+    const int e = active[is_item / ipe];
+    const int64_t i0 = (int64_t)(is_item % ipe) * 8;
+    is_gate = w13 + ((int64_t)e * 2 * I + i0 + cl.rpar) * H + cl.col * 16;
+  };
+  issue_item();
+  const int64_t up_off = I * H, two_rows = 2 * H;
+  auto issue = [&]() {
+    if (is_item < it_hi) {
+      const int kb0 = is_st * kStageKB;
+      if (kb0 + 1 < nkb || cl.col < 8) {
+        uint8_t *dst = ring + is_slot * kStageBytes + cl.soff;
+        const uint8_t *src = is_gate + kb0 * 128;
+#pragma unroll
+        for (int m = 0; m < 4; ++m) cp_async16(dst + m * 256, src + m * two_rows);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) cp_async16(dst + (m + 4) * 256, src + up_off + m * two_rows);
+      }
+      if (++is_slot == kRing) is_slot = 0;
+      if (++is_st == nst) {
+        is_st = 0;
+        if (++is_item < it_hi) issue_item();
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int st = 0; st < kRing - 1; ++st) issue();
+
+  // ---- consumer
+  const int f0 = stage_off(0, g, q), f1 = stage_off(0, g, 4 + q);  // rows g; rows g + 8 at +1024
+  float tot[NT][4];
+  int64_t cnt = 0, seg = 0, i0 = 0;
+  const float *sg = nullptr, *su = nullptr;
+  const __half *xrow[NT];
+  uint4 xn[4];
+  int slot = 0;
+  for (int item = it_lo; item < it_hi; ++item) {
+    {
+      const int e = active[item / ipe];
+      i0 = (int64_t)(item % ipe) * 8;
+      cnt = counts[e] - tb0;
+      seg = offsets[e] + tb0;
+      sg = s13 + ((int64_t)e * srow + i0 / 128) * nkb;
+      su = s13 + ((int64_t)e * srow + (I + i0) / 128) * nkb;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int64_t ti = j * 8 + g;
+        xrow[j] = (ti < cnt) ? x16 + (int64_t)(perm[seg + ti] / k) * H + q * 16 : nullptr;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) tot[j][v] = 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        xn[u] = xrow[0] ? ld_ro16(xrow[0] + (u >> 1) * 64 + (u & 1) * 8) : make_uint4(0, 0, 0, 0);
+    }
+    for (int st = 0; st < nst; ++st) {
+      __syncwarp();  // every lane is done reading the slot that is refilled next
+      issue();
+      cp_async_wait<kRing - 1>();
+      __syncwarp();
+      const uint8_t *sw = ring + slot * kStageBytes;
+      if (++slot == kRing) slot = 0;
+      const int kb0 = st * kStageKB;
+      const int nkbl = (nkb - kb0) < kStageKB ? (nkb - kb0) : kStageKB;
+      for (int kbl = 0; kbl < nkbl; ++kbl) {
+        const int kb = kb0 + kbl;
+        const float scg = __ldg(sg + kb), scu = __ldg(su + kb);
+        uint4 x0[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x0[u] = xn[u];
+        if (kb + 1 < nkb && xrow[0] != nullptr) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            xn[u] = ld_ro16(xrow[0] + (kb + 1) * 128 + (u >> 1) * 64 + (u & 1) * 8);
+        }
+        uint32_t a[2][4][4];
+        stage_fragments(sw + kbl * 2048, f0, f1, a);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          if (j * 8 >= cnt) break;
+          uint4 xc[4];
+          if (j == 0) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) xc[u] = x0[u];
+          } else if (xrow[j] != nullptr) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) xc[u] = ld_ro16(xrow[j] + kb * 128 + (u >> 1) * 64 + (u & 1) * 8);
+          } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) xc[u] = make_uint4(0, 0, 0, 0);
+          }
+          float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // two MMA chains
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              mma_16816(acc[c], a[c][s4][0], a[c][s4][1], a[c][s4][2], a[c][s4][3],
+                        u4_word(xc[2 * c + (s4 >> 1)], (2 * s4) & 3),
+                        u4_word(xc[2 * c + (s4 >> 1)], (2 * s4 + 1) & 3));
+          tot[j][0] = fmaf(acc[0][0] + acc[1][0], scg, tot[j][0]);
+          tot[j][1] = fmaf(acc[0][1] + acc[1][1], scg, tot[j][1]);
+          tot[j][2] = fmaf(acc[0][2] + acc[1][2], scu, tot[j][2]);
+          tot[j][3] = fmaf(acc[0][3] + acc[1][3], scu, tot[j][3]);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int d = 0; d < 2; ++d) {
+        const int64_t ti = j * 8 + 2 * q + d;
+        if (ti >= cnt) continue;
+        const int64_t pos = seg + ti;
+        const float xs = xscale[perm[pos] / k];
+        const float hv = swiglu(tot[j][d] * xs, tot[j][2 + d] * xs);
+        h[pos * I + i0 + g] = hv;
+        atomicMax(&hmax[pos], __float_as_uint(fabsf(hv)));
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// ---------------------------------------------------------------- W2
+// Item = (active expert, 16 consecutive output rows j0..j0+15), one warp, all
+// of K = I.  The activations h (f32, read through L1) are split into an f16
+// pair hi + lo after an exact power-of-two scaling chosen from the position's
+// largest |h|, so the products keep about 22 bits of h.
+template <int NT>
+__global__ void __launch_bounds__(32 * kGemvWarps) gemv2_kernel(
     const uint8_t *__restrict__ w2, const float *__restrict__ s2, const float *__restrict__ h,
     const uint32_t *__restrict__ hmax, const int32_t *__restrict__ counts,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ active,
-    const int32_t *__restrict__ n_active, int64_t H, int64_t I, float *__restrict__ y) {
-  __shared__ float red[4][32][NT][4];
+    const int32_t *__restrict__ n_active, int64_t H, int64_t I, int64_t tb0,
+    float *__restrict__ y) {
+  extern __shared__ __align__(128) uint8_t ring_all[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
-  const int tile = wid & 3, half = wid >> 2;
-  const int64_t nkb = I / 128;
-  const int64_t kb_mid = (nkb + 1) / 2;
-  const int64_t kb_begin = half ? kb_mid : 0, kb_end = half ? nkb : kb_mid;
-  const int64_t items_per_expert = H / 64;
-  const int64_t n_items = (int64_t)(*n_active) * items_per_expert;
+  uint8_t *ring = ring_all + wid * (kRing * kStageBytes);
+  const int ipe = (int)(H / 16);
+  const int nkb = (int)(I / 128);
+  const int nst = (nkb + kStageKB - 1) / kStageKB;
+  int it_lo, it_hi;
+  warp_items(*n_active * ipe, &it_lo, &it_hi);
+  if (it_lo >= it_hi) return;
 
-  for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int e = active[item / items_per_expert];
-    const int64_t j0 = (item % items_per_expert) * 64 + tile * 16;
-    const int64_t cnt = counts[e], seg = offsets[e];
-    const uint8_t *wa_row = w2 + ((int64_t)e * H + j0 + g) * I + q * 16;
-    const uint8_t *wb_row = w2 + ((int64_t)e * H + j0 + 8 + g) * I + q * 16;
-    const float *sc = s2 + ((int64_t)e * (H / 128) + j0 / 128) * nkb;
+  const CopyLane cl = copy_lane(lane);
+  int is_item = it_lo, is_st = 0, is_slot = 0;
+  const uint8_t *is_row = nullptr;
+  auto issue_item = [&]() {
+    const int e = active[is_item / ipe];
+    const int64_t j0 = (int64_t)(is_item % ipe) * 16;
+    is_row = w2 + ((int64_t)e * H + j0 + cl.rpar) * I + cl.col * 16;
+  };
+  issue_item();
+  const int64_t two_rows = 2 * I;
+  auto issue = [&]() {
+    if (is_item < it_hi) {
+      const int kb0 = is_st * kStageKB;
+      if (kb0 + 1 < nkb || cl.col < 8) {
+        uint8_t *dst = ring + is_slot * kStageBytes + cl.soff;
+        const uint8_t *src = is_row + kb0 * 128;
+#pragma unroll
+        for (int m = 0; m < 8; ++m) cp_async16(dst + m * 256, src + m * two_rows);
+      }
+      if (++is_slot == kRing) is_slot = 0;
+      if (++is_st == nst) {
+        is_st = 0;
+        if (++is_item < it_hi) issue_item();
+      }
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int st = 0; st < kRing - 1; ++st) issue();
 
-    for (int64_t tb = 0; tb < cnt; tb += NT * 8) {
-      const float *hrow[NT];
-      float down[NT];
+  const int f0 = stage_off(0, g, q), f1 = stage_off(0, g, 4 + q);
+  float tot[NT][4];
+  int64_t j0 = 0, cnt = 0, seg = 0;
+  const float *sc = nullptr;
+  const float *hrow[NT];
+  float down[NT];
+  int slot = 0;
+  for (int item = it_lo; item < it_hi; ++item) {
+    {
+      const int e = active[item / ipe];
+      j0 = (int64_t)(item % ipe) * 16;
+      cnt = counts[e] - tb0;
+      seg = offsets[e] + tb0;
+      sc = s2 + ((int64_t)e * (H / 128) + j0 / 128) * nkb;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        const int64_t ti = tb + j * 8 + g;
+        const int64_t ti = j * 8 + g;
         hrow[j] = (ti < cnt) ? h + (seg + ti) * I + q * 16 : nullptr;
         down[j] = (ti < cnt) ? exp2i(-f16_range_shift(__uint_as_float(hmax[seg + ti]))) : 0.f;
-      }
-      float tot[NT][4];
-#pragma unroll
-      for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int v = 0; v < 4; ++v) tot[j][v] = 0.f;
-
-      uint4 ca0, ca1, cb0, cb1;
-      if (kb_begin < kb_end) {
-        ca0 = ld_stream16(wa_row + kb_begin * 128);
-        ca1 = ld_stream16(wa_row + kb_begin * 128 + 64);
-        cb0 = ld_stream16(wb_row + kb_begin * 128);
-        cb1 = ld_stream16(wb_row + kb_begin * 128 + 64);
       }
-      for (int64_t kb = kb_begin; kb < kb_end; ++kb) {
-        uint4 na0, na1, nb0, nb1;
-        if (kb + 1 < kb_end) {
-          na0 = ld_stream16(wa_row + (kb + 1) * 128);
-          na1 = ld_stream16(wa_row + (kb + 1) * 128 + 64);
-          nb0 = ld_stream16(wb_row + (kb + 1) * 128);
-          nb1 = ld_stream16(wb_row + (kb + 1) * 128 + 64);
-        }
-        float acc[NT][4];
+    }
+    for (int st = 0; st < nst; ++st) {
+      __syncwarp();
+      issue();
+      cp_async_wait<kRing - 1>();
+      __syncwarp();
+      const uint8_t *sw = ring + slot * kStageBytes;
+      if (++slot == kRing) slot = 0;
+      const int kb0 = st * kStageKB;
+      const int nkbl = (nkb - kb0) < kStageKB ? (nkb - kb0) : kStageKB;
+      for (int kbl = 0; kbl < nkbl; ++kbl) {
+        const int kb = kb0 + kbl;
+        const float sck = __ldg(sc + kb);
+        uint32_t a[2][4][4];
+        stage_fragments(sw + kbl * 2048, f0, f1, a);
 #pragma unroll
-        for (int j = 0; j < NT; ++j)
+        for (int j = 0; j < NT; ++j) {
+          if (j * 8 >= cnt) break;
+          float acc[4] = {0.f, 0.f, 0.f, 0.f}, acl[4] = {0.f, 0.f, 0.f, 0.f};  // hi and lo chains
 #pragma unroll
-          for (int v = 0; v < 4; ++v) acc[j][v] = 0.f;
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint4 wa = c ? ca1 : ca0, wb = c ? cb1 : cb0;
-          uint32_t bhi[NT][8], blo[NT][8];
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
+          for (int c = 0; c < 2; ++c) {
+            uint32_t bhi[8], blo[8];
             if (hrow[j] != nullptr) {
               const float4 *src = reinterpret_cast<const float4 *>(hrow[j] + kb * 128 + c * 64);
 #pragma unroll
@@ -238,62 +362,40 @@ __global__ void __launch_bounds__(256) gemv2_kernel(
                 v.x *= down[j]; v.y *= down[j]; v.z *= down[j]; v.w *= down[j];
                 const uint32_t h0 = pack_f16x2(v.x, v.y), h1 = pack_f16x2(v.z, v.w);
                 const float2 r0 = unpack_f16x2(h0), r1 = unpack_f16x2(h1);
-                bhi[j][2 * m] = h0;
-                bhi[j][2 * m + 1] = h1;
-                blo[j][2 * m] = pack_f16x2(v.x - r0.x, v.y - r0.y);
-                blo[j][2 * m + 1] = pack_f16x2(v.z - r1.x, v.w - r1.y);
+                bhi[2 * m] = h0;
+                bhi[2 * m + 1] = h1;
+                blo[2 * m] = pack_f16x2(v.x - r0.x, v.y - r0.y);
+                blo[2 * m + 1] = pack_f16x2(v.z - r1.x, v.w - r1.y);
               }
             } else {
 #pragma unroll
-              for (int m = 0; m < 8; ++m) { bhi[j][m] = 0u; blo[j][m] = 0u; }
+              for (int m = 0; m < 8; ++m) { bhi[m] = 0u; blo[m] = 0u; }
+            }
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4) {
+              mma_16816(acc, a[c][s4][0], a[c][s4][1], a[c][s4][2], a[c][s4][3], bhi[2 * s4], bhi[2 * s4 + 1]);
+              mma_16816(acl, a[c][s4][0], a[c][s4][1], a[c][s4][2], a[c][s4][3], blo[2 * s4], blo[2 * s4 + 1]);
             }
           }
 #pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint32_t aw = u4_word(wa, s), bw = u4_word(wb, s);
-            const uint32_t a0 = e4m3x2_to_f16x2(aw & 0xffffu);
-            const uint32_t a1 = e4m3x2_to_f16x2(bw & 0xffffu);
-            const uint32_t a2 = e4m3x2_to_f16x2(aw >> 16);
-            const uint32_t a3 = e4m3x2_to_f16x2(bw >> 16);
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              mma_16816(acc[j], a0, a1, a2, a3, bhi[j][2 * s], bhi[j][2 * s + 1]);
-              mma_16816(acc[j], a0, a1, a2, a3, blo[j][2 * s], blo[j][2 * s + 1]);
-            }
-          }
-        }
-        const float sck = __ldg(sc + kb);
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) tot[j][v] = fmaf(acc[j][v], sck, tot[j][v]);
-        ca0 = na0; ca1 = na1; cb0 = nb0; cb1 = nb1;
-      }
-
-      if (half == 1) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) red[tile][lane][j][v] = tot[j][v];
-      }
-      __syncthreads();
-      if (half == 0) {
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-#pragma unroll
-          for (int d = 0; d < 2; ++d) {
-            const int64_t ti = tb + j * 8 + 2 * q + d;
-            if (ti >= cnt) continue;
-            const int64_t pos = seg + ti;
-            const float up = exp2i(f16_range_shift(__uint_as_float(hmax[pos])));
-            y[pos * H + j0 + g] = (tot[j][d] + red[tile][lane][j][d]) * up;
-            y[pos * H + j0 + 8 + g] = (tot[j][2 + d] + red[tile][lane][j][2 + d]) * up;
-          }
+          for (int v = 0; v < 4; ++v) tot[j][v] = fmaf(acc[v] + acl[v], sck, tot[j][v]);
         }
       }
-      __syncthreads();
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+#pragma unroll
+      for (int d = 0; d < 2; ++d) {
+        const int64_t ti = j * 8 + 2 * q + d;
+        if (ti >= cnt) continue;
+        const int64_t pos = seg + ti;
+        const float up = exp2i(f16_range_shift(__uint_as_float(hmax[pos])));
+        y[pos * H + j0 + g] = tot[j][d] * up;
+        y[pos * H + j0 + 8 + g] = tot[j][2 + d] * up;
+      }
     }
   }
+  cp_async_wait<0>();
 }
 
 // ---------------------------------------------------------------- combine
@@ -330,34 +432,77 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
 
 // ---------------------------------------------------------------- launchers
 
+namespace {
+template <typename K>
+cudaError_t allow_smem(K kernel, size_t smem) {
+  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+constexpr size_t kGemvSmem = (size_t)kGemvWarps * kRing * kStageBytes;
+// grid: enough warps for every item, but never more CTAs than fit on the GPU
+// at once (each warp owns a fixed item range, so a second wave would run late)
+template <typename K>
+int64_t gemv_grid(K kernel, int64_t max_items, int sms) {
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 32 * kGemvWarps, kGemvSmem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t g = (max_items + kGemvWarps - 1) / kGemvWarps;
+  const int64_t cap = (int64_t)sms * per_sm;
+  return g < cap ? g : cap;
+}
+}  // namespace
+
+// Token groups of up to 8 * NT per pass; T <= 8 needs one group (NT = 1),
+// T <= 64 fits in NT = 8; larger T runs ceil(T / 64) passes of 64 tokens.
 cudaError_t launch_gemv13(const uint8_t *w13, const float *s13, const __half *x16,
                           const float *xscale, const int32_t *counts, const int32_t *offsets,
                           const int32_t *perm, const int32_t *active, const int32_t *n_active,
-                          int k, int64_t H, int64_t I, float *h, uint32_t *hmax, int64_t max_items,
-                          int wide_tokens, int grid_cap, cudaStream_t s) {
-  const int64_t grid = max_items < grid_cap ? max_items : grid_cap;
+                          int k, int64_t T, int64_t H, int64_t I, float *h, uint32_t *hmax,
+                          int64_t max_items, int *err, int sms, cudaStream_t s) {
+  cudaError_t e;
+  if (T <= 8) {
+    auto kern = gemv13_swiglu_kernel<1>;
+    if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
+    const int64_t grid = gemv_grid(kern, max_items, sms);
+    if (grid <= 0) return cudaSuccess;
+    kern<<<(unsigned)grid, 32 * kGemvWarps, kGemvSmem, s>>>(w13, s13, x16, xscale, counts, offsets,
+                                                            perm, active, n_active, k, H, I, 0, h,
+                                                            hmax);
+    return cudaGetLastError();
+  }
+  auto kern = gemv13_swiglu_kernel<8>;
+  if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
+  const int64_t grid = gemv_grid(kern, max_items, sms);
   if (grid <= 0) return cudaSuccess;
-  if (wide_tokens)
-    gemv13_swiglu_kernel<4><<<(unsigned)grid, 256, 0, s>>>(w13, s13, x16, xscale, counts, offsets,
-                                                           perm, active, n_active, k, H, I, h, hmax);
-  else
-    gemv13_swiglu_kernel<1><<<(unsigned)grid, 256, 0, s>>>(w13, s13, x16, xscale, counts, offsets,
-                                                           perm, active, n_active, k, H, I, h, hmax);
+  for (int64_t tb0 = 0; tb0 < T; tb0 += 64)
+    kern<<<(unsigned)grid, 32 * kGemvWarps, kGemvSmem, s>>>(w13, s13, x16, xscale, counts, offsets,
+                                                            perm, active, n_active, k, H, I, tb0, h,
+                                                            hmax);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, const uint32_t *hmax,
                          const int32_t *counts, const int32_t *offsets, const int32_t *active,
-                         const int32_t *n_active, int64_t H, int64_t I, float *y,
-                         int64_t max_items, int wide_tokens, int grid_cap, cudaStream_t s) {
-  const int64_t grid = max_items < grid_cap ? max_items : grid_cap;
+                         const int32_t *n_active, int64_t T, int64_t H, int64_t I, float *y,
+                         int64_t max_items, int *err, int sms, cudaStream_t s) {
+  cudaError_t e;
+  if (T <= 8) {
+    auto kern = gemv2_kernel<1>;
+    if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
+    const int64_t grid = gemv_grid(kern, max_items, sms);
+    if (grid <= 0) return cudaSuccess;
+    kern<<<(unsigned)grid, 32 * kGemvWarps, kGemvSmem, s>>>(w2, s2, h, hmax, counts, offsets,
+                                                            active, n_active, H, I, 0, y);
+    return cudaGetLastError();
+  }
+  auto kern = gemv2_kernel<8>;
+  if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
+  const int64_t grid = gemv_grid(kern, max_items, sms);
   if (grid <= 0) return cudaSuccess;
-  if (wide_tokens)
-    gemv2_kernel<4><<<(unsigned)grid, 256, 0, s>>>(w2, s2, h, hmax, counts, offsets, active,
-                                                   n_active, H, I, y);
-  else
-    gemv2_kernel<1><<<(unsigned)grid, 256, 0, s>>>(w2, s2, h, hmax, counts, offsets, active,
-                                                   n_active, H, I, y);
+  for (int64_t tb0 = 0; tb0 < T; tb0 += 64)
+    kern<<<(unsigned)grid, 32 * kGemvWarps, kGemvSmem, s>>>(w2, s2, h, hmax, counts, offsets,
+                                                            active, n_active, H, I, tb0, y);
   return cudaGetLastError();
 }
 

@@ -15,31 +15,37 @@ constexpr int64_t kRouterWarpMaxT = 64;
 // Rows of one grouped-GEMM tile (tile list granularity).
 constexpr int kTileM = 128;
 
-int router_chain_depth(int64_t T, int64_t H);
+// Largest split of the router's K loop over CTAs (planes of partial logits).
+constexpr int kRouterMaxKSplit = 8;
+int router_k_split(int64_t T, int64_t E, int64_t H, int sms);
+int router_chain_depth(int64_t T, int64_t H, int ks);
 cudaError_t launch_router_logits(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
-                                 int64_t H, float *logits, float *wnorm, cudaStream_t s);
+                                 int64_t H, int ks, float *logits, float *wnorm, cudaStream_t s);
 size_t router_select_smem(int64_t E);
 cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float *W,
                                  const float *bias, int64_t E, int64_t H, int k,
-                                 const float *logits, const float *wnorm, float gamma_d,
+                                 const float *logits, const float *wnorm, int ks, float gamma_d,
                                  int32_t *idx, float *wts, __half *x16, float *xscale, int *err,
                                  cudaStream_t s);
 
 size_t permute_smem(int E);
+// Also clears pos_max[P] (if given) and the n_counters work counters.
 cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int tile_m, int32_t *counts,
                            int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *active,
-                           int32_t *n_active, int32_t *tile_offsets, uint32_t *pos_max, int *err,
-                           cudaStream_t s);
+                           int32_t *n_active, int32_t *tile_offsets, uint32_t *pos_max,
+                           int32_t *counters, int n_counters, int *err, cudaStream_t s);
 
+// Decode grouped GEMVs over the active experts' weight rows; T bounds the
+// tokens any expert can hold (passes of 64 tokens above 64).
 cudaError_t launch_gemv13(const uint8_t *w13, const float *s13, const __half *x16,
                           const float *xscale, const int32_t *counts, const int32_t *offsets,
                           const int32_t *perm, const int32_t *active, const int32_t *n_active,
-                          int k, int64_t H, int64_t I, float *h, uint32_t *hmax, int64_t max_items,
-                          int wide_tokens, int grid_cap, cudaStream_t s);
+                          int k, int64_t T, int64_t H, int64_t I, float *h, uint32_t *hmax,
+                          int64_t max_items, int *err, int sms, cudaStream_t s);
 cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, const uint32_t *hmax,
                          const int32_t *counts, const int32_t *offsets, const int32_t *active,
-                         const int32_t *n_active, int64_t H, int64_t I, float *y,
-                         int64_t max_items, int wide_tokens, int grid_cap, cudaStream_t s);
+                         const int32_t *n_active, int64_t T, int64_t H, int64_t I, float *y,
+                         int64_t max_items, int *err, int sms, cudaStream_t s);
 bool encode_u8_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows);
 cudaError_t launch_act_quant(const __nv_bfloat16 *x, const int32_t *perm, int64_t P, int k,
                              int64_t H, int64_t Pmax, uint8_t *a_hi, uint8_t *a_lo, float *a_scale,

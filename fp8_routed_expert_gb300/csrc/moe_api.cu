@@ -33,6 +33,7 @@ struct moe_ctx {
   float *h = nullptr, *y = nullptr;
   int32_t *idx = nullptr, *counts = nullptr, *offsets = nullptr, *perm = nullptr, *inv = nullptr;
   int32_t *active = nullptr, *n_active = nullptr, *tile_offsets = nullptr;
+  int32_t *work_ctr = nullptr;  // dynamic item counters of the GEMV kernels
   uint32_t *hmax = nullptr;
   __half *x16 = nullptr;
   __nv_bfloat16 *xin = nullptr, *xout = nullptr;  // staging for the host-buffer entry point
@@ -72,9 +73,9 @@ int check_config(const moe_config *c) {
   return MOE_OK;
 }
 
-float router_gamma(int64_t T, int64_t H) {
+float router_gamma(int64_t T, int64_t H, int ks) {
   const double u = std::ldexp(1.0, -24);
-  const double d = (double)router_chain_depth(T, H);
+  const double d = (double)router_chain_depth(T, H, ks);
   const double g = d * u / (1.0 - d * u);
   return std::nextafter((float)(g * (1.0 + 1e-6)), INFINITY);
 }
@@ -138,13 +139,15 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
   int path = c->path != MOE_PATH_AUTO ? c->path : (T <= kGemvMaxT ? MOE_PATH_GEMV : MOE_PATH_GEMM);
   if (path == MOE_PATH_GEMM && H % 256 != 0) path = MOE_PATH_GEMV;  // GEMM2 tiles are 256 wide
   const int64_t max_active = P < E ? P : E;
+  const int ks = router_k_split(T, E, H, c->sms);
   {
     Timed tm(c, MOE_K_ROUTER_LOGITS, s);
-    CUDA_TRY(launch_router_logits(x, T, rw, E, H, c->logits, c->wnorm, s));
+    CUDA_TRY(launch_router_logits(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
   }
   {
     Timed tm(c, MOE_K_ROUTER_SELECT, s);
-    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, router_gamma(T, H),
+    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks,
+                                  router_gamma(T, H, ks),
                                   c->idx, c->wts, path == MOE_PATH_GEMV ? c->x16 : nullptr,
                                   c->xscale, c->err, s));
   }
@@ -152,20 +155,19 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
     Timed tm(c, MOE_K_PERMUTE, s);
     CUDA_TRY(launch_permute(c->idx, P, (int)E, kTileM, c->counts, c->offsets, c->perm, c->inv,
                             c->active, c->n_active, c->tile_offsets,
-                            path == MOE_PATH_GEMV ? c->hmax : nullptr, c->err, s));
+                            path == MOE_PATH_GEMV ? c->hmax : nullptr, c->work_ctr, 2, c->err, s));
   }
   if (path == MOE_PATH_GEMV) {
-    const int wide = T > kGemvMaxT ? 1 : 0;
     {
       Timed tm(c, MOE_K_GATE_UP, s);
       CUDA_TRY(launch_gemv13(w13, s13, c->x16, c->xscale, c->counts, c->offsets, c->perm,
-                             c->active, c->n_active, k, H, I, c->h, c->hmax,
-                             max_active * (I / 32), wide, c->sms * 4, s));
+                             c->active, c->n_active, k, T, H, I, c->h, c->hmax,
+                             max_active * (I / 8), c->err, c->sms, s));
     }
     {
       Timed tm(c, MOE_K_DOWN, s);
-      CUDA_TRY(launch_gemv2(w2, s2, c->h, c->hmax, c->counts, c->offsets, c->active, c->n_active,
-                            H, I, c->y, max_active * (H / 64), wide, c->sms * 4, s));
+      CUDA_TRY(launch_gemv2(w2, s2, c->h, c->hmax, c->counts, c->offsets, c->active, c->n_active, T,
+                            H, I, c->y, max_active * (H / 16), c->err, c->sms, s));
     }
   } else {
     if (c->tm_w13_ptr != w13) {
@@ -273,7 +275,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
     void **p;
     size_t bytes;
   } slots[] = {
-      {(void **)&c->logits, (size_t)(Tm * E) * 4},
+      {(void **)&c->logits, (size_t)(kRouterMaxKSplit * Tm * E) * 4},
       {(void **)&c->wnorm, (size_t)E * 4},
       {(void **)&c->idx, (size_t)Pm * 4},
       {(void **)&c->wts, (size_t)Pm * 4},
@@ -283,6 +285,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->inv, (size_t)Pm * 4},
       {(void **)&c->active, (size_t)E * 4},
       {(void **)&c->n_active, 16},
+      {(void **)&c->work_ctr, 16},
       {(void **)&c->tile_offsets, (size_t)(E + 1) * 4},
       {(void **)&c->hmax, (size_t)Pm * 4},
       {(void **)&c->x16, (size_t)(Tm * H) * 2},

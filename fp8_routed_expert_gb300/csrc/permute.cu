@@ -52,7 +52,8 @@ __global__ void __launch_bounds__(1024) permute_kernel(
     const int32_t *__restrict__ idx, int64_t P, int E, int tile_m, int32_t *__restrict__ counts,
     int32_t *__restrict__ offsets, int32_t *__restrict__ perm, int32_t *__restrict__ inv,
     int32_t *__restrict__ active, int32_t *__restrict__ n_active,
-    int32_t *__restrict__ tile_offsets, uint32_t *__restrict__ pos_max, int *__restrict__ err) {
+    int32_t *__restrict__ tile_offsets, uint32_t *__restrict__ pos_max,
+    int32_t *__restrict__ counters, int n_counters, int *__restrict__ err) {
   extern __shared__ int sm[];
   int *whist = sm;                 // [32][E]
   int *seg = sm + 32 * E;          // [E+1] segment starts
@@ -61,6 +62,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
 
   for (int i = tid; i < 32 * E; i += blockDim.x) whist[i] = 0;
+  if (tid < n_counters) counters[tid] = 0;
   if (pos_max != nullptr)
     for (int64_t p = tid; p < P; p += blockDim.x) pos_max[p] = 0u;
   __syncthreads();
@@ -136,8 +138,8 @@ size_t permute_smem(int E) { return (size_t)(33 * E + 1) * sizeof(int); }
 
 cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int tile_m, int32_t *counts,
                            int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *active,
-                           int32_t *n_active, int32_t *tile_offsets, uint32_t *pos_max, int *err,
-                           cudaStream_t s) {
+                           int32_t *n_active, int32_t *tile_offsets, uint32_t *pos_max,
+                           int32_t *counters, int n_counters, int *err, cudaStream_t s) {
   const size_t smem = permute_smem(E);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(permute_kernel,
@@ -145,7 +147,7 @@ cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int tile_m, int
     if (e != cudaSuccess) return e;
   }
   permute_kernel<<<1, 1024, smem, s>>>(idx, P, E, tile_m, counts, offsets, perm, inv, active,
-                                       n_active, tile_offsets, pos_max, err);
+                                       n_active, tile_offsets, pos_max, counters, n_counters, err);
   return cudaGetLastError();
 }
 

@@ -98,6 +98,12 @@ __global__ void __launch_bounds__(256) router_logits_split_kernel(
 __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
     const __nv_bfloat16 *__restrict__ x, int64_t T, const float *__restrict__ W, int64_t E,
     int64_t H, float *__restrict__ logits) {
+  // blockIdx.z selects a contiguous range of K blocks; its partial logits go
+  // to plane z of logits [KS][T][E] and the select kernel adds the planes in
+  // order (KS - 1 more roundings in the chain).
+  const int64_t nkb_all = H / 128, ks = gridDim.z, z = blockIdx.z;
+  const int64_t kb_lo = nkb_all * z / ks, kb_hi = nkb_all * (z + 1) / ks;
+  logits += z * T * E;
   __shared__ __align__(16) float xs[32][68];
   __shared__ __align__(16) float ws[32][68];
   const int tid = threadIdx.x;
@@ -111,7 +117,7 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
 
   const int lr = tid >> 2;        // row of the tile this thread stages (0..63)
   const int lk = (tid & 3) * 8;   // first of its 8 k values
-  for (int64_t kb = 0; kb < H; kb += 128) {
+  for (int64_t kb = kb_lo * 128; kb < kb_hi * 128; kb += 128) {
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
@@ -224,7 +230,7 @@ __device__ __forceinline__ int warp_argmax(int E, uint32_t taken, F key, K *best
 __global__ void __launch_bounds__(128) router_select_kernel(
     const __nv_bfloat16 *__restrict__ x, int64_t T, const float *__restrict__ W,
     const float *__restrict__ bias, int64_t E, int64_t H, int k, const float *__restrict__ logits,
-    const float *__restrict__ wnorm, float gamma_d, int32_t *__restrict__ idx,
+    const float *__restrict__ wnorm, int ks, float gamma_d, int32_t *__restrict__ idx,
     float *__restrict__ wts, __half *__restrict__ x16, float *__restrict__ xscale,
     int *__restrict__ err) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -267,6 +273,7 @@ __global__ void __launch_bounds__(128) router_select_kernel(
   bool finite = true;
   for (int e = lane; e < E; e += 32) {
     float v = logits[t * E + e];
+    for (int z = 1; z < ks; ++z) v += logits[(z * T + t) * E + e];
     if (bias != nullptr) v += bias[e];
     finite = finite && isfinite(v);
     lg[e] = v;
@@ -335,11 +342,20 @@ __global__ void __launch_bounds__(128) router_select_kernel(
     if ((be & 31) == lane) taken2 |= 1u << (be >> 5);
     kth_lo = bv;
   }
-  for (int e = 0; e < E; ++e) {
-    // uniform across the warp: every lane evaluates the same condition
-    const bool cand = !(key32(e) + beta(e) < kth_lo) && isfinite(lg[e]);
-    double v = -INFINITY;
-    if (cand) {
+  // candidates: each lane tests its own experts; the warp then recomputes
+  // them one at a time (lane order, then j), all lanes cooperating on the dot
+  uint32_t cmask = 0;
+  for (int j = 0; lane + 32 * j < E; ++j) {
+    const int e = lane + 32 * j;
+    if (!(key32(e) + beta(e) < kth_lo) && isfinite(lg[e])) cmask |= 1u << j;
+    else lg64[e] = -INFINITY;
+  }
+  for (int src = 0; src < 32; ++src) {
+    uint32_t m = __shfl_sync(0xffffffffu, cmask, src);
+    while (m != 0u) {
+      const int j = __ffs(m) - 1;
+      m &= m - 1u;
+      const int e = src + 32 * j;
       const float *w = W + (int64_t)e * H;
       double acc = 0.0;
       for (int64_t h = 4 * lane; h < H; h += 128) {
@@ -350,10 +366,10 @@ __global__ void __launch_bounds__(128) router_select_kernel(
         acc = fma((double)bf16_bits_to_float(xv.y & 0xffffu), (double)wv.z, acc);
         acc = fma((double)bf16_bits_to_float(xv.y >> 16), (double)wv.w, acc);
       }
-      v = warp_sum(acc);
+      double v = warp_sum(acc);
       if (bias != nullptr) v += (double)bias[e];
+      if (lane == 0) lg64[e] = v;
     }
-    if (lane == 0) lg64[e] = v;
   }
   __syncwarp();
   auto key64 = [&](int e) -> double { return lg64[e]; };
@@ -378,12 +394,23 @@ __global__ void __launch_bounds__(128) router_select_kernel(
 
 // ------------------------------------------------------------------ launchers
 
-int router_chain_depth(int64_t T, int64_t H) {
-  return T <= kRouterWarpMaxT ? (int)(4 * ((H + 1023) / 1024) + 5 + 8 + 1) : (int)(128 + H / 128 + 1);
+int router_k_split(int64_t T, int64_t E, int64_t H, int sms) {
+  if (T <= kRouterWarpMaxT) return 1;
+  const int64_t tiles = ((T + 63) / 64) * ((E + 63) / 64);
+  int64_t ks = (2 * sms + tiles - 1) / tiles;
+  const int64_t nkb = H / 128;
+  if (ks > nkb) ks = nkb;
+  if (ks > kRouterMaxKSplit) ks = kRouterMaxKSplit;
+  return ks < 1 ? 1 : (int)ks;
+}
+
+int router_chain_depth(int64_t T, int64_t H, int ks) {
+  return T <= kRouterWarpMaxT ? (int)(4 * ((H + 1023) / 1024) + 5 + 8 + 1)
+                              : (int)(128 + H / 128 + ks + 1);
 }
 
 cudaError_t launch_router_logits(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
-                                 int64_t H, float *logits, float *wnorm, cudaStream_t s) {
+                                 int64_t H, int ks, float *logits, float *wnorm, cudaStream_t s) {
   if (T <= kRouterWarpMaxT) {
     if (T <= 1)
       router_logits_split_kernel<1><<<(unsigned)E, 256, 0, s>>>(x, T, W, E, H, logits, wnorm);
@@ -392,7 +419,7 @@ cudaError_t launch_router_logits(const __nv_bfloat16 *x, int64_t T, const float 
     return cudaGetLastError();
   }
   row_norm_kernel<<<(unsigned)((E + 3) / 4), 128, 0, s>>>(W, E, H, wnorm);
-  dim3 grid((unsigned)((E + 63) / 64), (unsigned)((T + 63) / 64));
+  dim3 grid((unsigned)((E + 63) / 64), (unsigned)((T + 63) / 64), (unsigned)ks);
   router_logits_tiled_kernel<<<grid, 256, 0, s>>>(x, T, W, E, H, logits);
   return cudaGetLastError();
 }
@@ -401,7 +428,7 @@ size_t router_select_smem(int64_t E) { return (size_t)4 * E * (sizeof(double) + 
 
 cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float *W,
                                  const float *bias, int64_t E, int64_t H, int k,
-                                 const float *logits, const float *wnorm, float gamma_d,
+                                 const float *logits, const float *wnorm, int ks, float gamma_d,
                                  int32_t *idx, float *wts, __half *x16, float *xscale, int *err,
                                  cudaStream_t s) {
   const size_t smem = router_select_smem(E);
@@ -411,7 +438,7 @@ cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float 
     if (e != cudaSuccess) return e;
   }
   router_select_kernel<<<(unsigned)((T + 3) / 4), 128, smem, s>>>(
-      x, T, W, bias, E, H, k, logits, wnorm, gamma_d, idx, wts, x16, xscale, err);
+      x, T, W, bias, E, H, k, logits, wnorm, ks, gamma_d, idx, wts, x16, xscale, err);
   return cudaGetLastError();
 }
 

@@ -176,3 +176,19 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 
 }  // namespace sm100
 }  // namespace fp8moe
+
+namespace fp8moe {
+namespace sm100 {
+
+// 1-D bulk copy global -> shared (TMA engine), `bytes` a multiple of 16, both
+// addresses 16-byte aligned; completes `bytes` on `bar`.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+}  // namespace sm100
+}  // namespace fp8moe
