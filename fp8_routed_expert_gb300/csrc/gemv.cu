@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv13_swiglu_kernel(
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
   uint8_t *ring = ring_all + wid * (kRing * kStageBytes);
+  pdl_wait();     // routing, x16 and the cleared maxima come from the previous kernel
+  pdl_trigger();
   const int ipe = (int)(I / 8);
   const int nkb = (int)(H / 128);
   const int nst = (nkb + kStageKB - 1) / kStageKB;
@@ -309,6 +311,10 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv2_kernel(
   };
 #pragma unroll
   for (int st = 0; st < kRing - 1; ++st) issue();
+  // the routing was complete before the previous kernel started; h and its
+  // maxima are that kernel's output
+  pdl_wait();
+  pdl_trigger();
 
   const int f0 = stage_off(0, g, q), f1 = stage_off(0, g, 4 + q);
   float tot[NT][4];
@@ -407,6 +413,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                                                       const float *__restrict__ wts, int64_t T,
                                                       int k, int64_t H,
                                                       __nv_bfloat16 *__restrict__ out) {
+  pdl_wait();
   const int64_t t = blockIdx.x;
   if (t >= T) return;
   for (int64_t j = 4 * (int64_t)(blockIdx.y * blockDim.x + threadIdx.x); j < H;
@@ -466,10 +473,8 @@ cudaError_t launch_gemv13(const uint8_t *w13, const float *s13, const __half *x1
     if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
     const int64_t grid = gemv_grid(kern, max_items, sms);
     if (grid <= 0) return cudaSuccess;
-    kern<<<(unsigned)grid, 32 * kGemvWarps, kGemvSmem, s>>>(w13, s13, x16, xscale, counts, offsets,
-                                                            perm, active, n_active, k, H, I, 0, h,
-                                                            hmax);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(32 * kGemvWarps), kGemvSmem, s, w13, s13, x16,
+                      xscale, counts, offsets, perm, active, n_active, k, H, I, (int64_t)0, h, hmax);
   }
   auto kern = gemv13_swiglu_kernel<8>;
   if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
@@ -492,9 +497,8 @@ cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, con
     if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
     const int64_t grid = gemv_grid(kern, max_items, sms);
     if (grid <= 0) return cudaSuccess;
-    kern<<<(unsigned)grid, 32 * kGemvWarps, kGemvSmem, s>>>(w2, s2, h, hmax, counts, offsets,
-                                                            active, n_active, H, I, 0, y);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(32 * kGemvWarps), kGemvSmem, s, w2, s2, h, hmax,
+                      counts, offsets, active, n_active, H, I, (int64_t)0, y);
   }
   auto kern = gemv2_kernel<8>;
   if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
@@ -508,9 +512,8 @@ cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, con
 
 cudaError_t launch_combine(const float *y, const int32_t *inv, const float *wts, int64_t T, int k,
                            int64_t H, __nv_bfloat16 *out, cudaStream_t s) {
-  dim3 grid((unsigned)T, (unsigned)((H + 1023) / 1024));
-  combine_kernel<<<grid, 256, 0, s>>>(y, inv, wts, T, k, H, out);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)T, (unsigned)((H + 1023) / 1024)), dim3(256), 0, s, y,
+                    inv, wts, T, k, H, out);
 }
 
 }  // namespace fp8moe

@@ -7,7 +7,27 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace fp8moe {
+
+// Launch with programmatic stream serialization (the kernel starts before
+// its predecessor finishes and orders itself with griddepcontrol.wait).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // T at or below which the router uses one warp per expert row; above it, the
 // tiled kernel.
@@ -19,14 +39,26 @@ constexpr int kTileM = 128;
 constexpr int kRouterMaxKSplit = 8;
 int router_k_split(int64_t T, int64_t E, int64_t H, int sms);
 int router_chain_depth(int64_t T, int64_t H, int ks);
-cudaError_t launch_router_logits(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
-                                 int64_t H, int ks, float *logits, float *wnorm, cudaStream_t s);
+// T <= kRouterWarpMaxT: logits, selection and the pair sort in one launch
+// (ticket: an int32 that is 0 between calls).
+size_t route_decode_smem(int64_t E);
+cudaError_t launch_route_decode(const __nv_bfloat16 *x, int64_t T, const float *W, const float *bias,
+                                int64_t E, int64_t H, int k, float gamma, float *logits, float *wnorm,
+                                float *xnorm, __half *x16, float *xscale, int32_t *ticket,
+                                int32_t *idx, float *wts, int32_t *counts, int32_t *offsets,
+                                int32_t *perm, int32_t *inv, int32_t *active, int32_t *n_active,
+                                int32_t *tile_offsets, int tile_m, uint32_t *pos_max, int *err,
+                                cudaStream_t s);
+// T > kRouterWarpMaxT: tiled logits (ks planes), then selection.
+cudaError_t launch_router_logits_tiled(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
+                                       int64_t H, int ks, float *logits, float *wnorm, cudaStream_t s);
+cudaError_t launch_x_to_f16(const __nv_bfloat16 *x, int64_t T, int64_t H, __half *x16, float *xscale,
+                           cudaStream_t s);
 size_t router_select_smem(int64_t E);
 cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float *W,
                                  const float *bias, int64_t E, int64_t H, int k,
                                  const float *logits, const float *wnorm, int ks, float gamma_d,
-                                 int32_t *idx, float *wts, __half *x16, float *xscale, int *err,
-                                 cudaStream_t s);
+                                 int32_t *idx, float *wts, int *err, cudaStream_t s);
 
 size_t permute_smem(int E);
 // Also clears pos_max[P] (if given) and the n_counters work counters.

@@ -33,7 +33,8 @@ struct moe_ctx {
   float *h = nullptr, *y = nullptr;
   int32_t *idx = nullptr, *counts = nullptr, *offsets = nullptr, *perm = nullptr, *inv = nullptr;
   int32_t *active = nullptr, *n_active = nullptr, *tile_offsets = nullptr;
-  int32_t *work_ctr = nullptr;  // dynamic item counters of the GEMV kernels
+  int32_t *ticket = nullptr;  // completion ticket of the fused routing kernel (0 between calls)
+  float *xnorm = nullptr;     // ||x_t||_2
   uint32_t *hmax = nullptr;
   __half *x16 = nullptr;
   __nv_bfloat16 *xin = nullptr, *xout = nullptr;  // staging for the host-buffer entry point
@@ -140,22 +141,31 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
   if (path == MOE_PATH_GEMM && H % 256 != 0) path = MOE_PATH_GEMV;  // GEMM2 tiles are 256 wide
   const int64_t max_active = P < E ? P : E;
   const int ks = router_k_split(T, E, H, c->sms);
-  {
-    Timed tm(c, MOE_K_ROUTER_LOGITS, s);
-    CUDA_TRY(launch_router_logits(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
-  }
-  {
-    Timed tm(c, MOE_K_ROUTER_SELECT, s);
-    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks,
-                                  router_gamma(T, H, ks),
-                                  c->idx, c->wts, path == MOE_PATH_GEMV ? c->x16 : nullptr,
-                                  c->xscale, c->err, s));
-  }
-  {
-    Timed tm(c, MOE_K_PERMUTE, s);
-    CUDA_TRY(launch_permute(c->idx, P, (int)E, kTileM, c->counts, c->offsets, c->perm, c->inv,
-                            c->active, c->n_active, c->tile_offsets,
-                            path == MOE_PATH_GEMV ? c->hmax : nullptr, c->work_ctr, 2, c->err, s));
+  const float gamma = router_gamma(T, H, ks);
+  if (T <= kRouterWarpMaxT) {
+    Timed tm(c, MOE_K_ROUTE, s);
+    CUDA_TRY(launch_route_decode(x, T, rw, rb, E, H, k, gamma, c->logits, c->wnorm, c->xnorm,
+                                 path == MOE_PATH_GEMV ? c->x16 : nullptr, c->xscale, c->ticket,
+                                 c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv, c->active,
+                                 c->n_active, c->tile_offsets, kTileM,
+                                 path == MOE_PATH_GEMV ? c->hmax : nullptr, c->err, s));
+  } else {
+    {
+      Timed tm(c, MOE_K_ROUTER_LOGITS, s);
+      CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
+    }
+    {
+      Timed tm(c, MOE_K_ROUTER_SELECT, s);
+      CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks, gamma, c->idx,
+                                    c->wts, c->err, s));
+    }
+    if (path == MOE_PATH_GEMV) CUDA_TRY(launch_x_to_f16(x, T, H, c->x16, c->xscale, s));
+    {
+      Timed tm(c, MOE_K_PERMUTE, s);
+      CUDA_TRY(launch_permute(c->idx, P, (int)E, kTileM, c->counts, c->offsets, c->perm, c->inv,
+                              c->active, c->n_active, c->tile_offsets,
+                              path == MOE_PATH_GEMV ? c->hmax : nullptr, nullptr, 0, c->err, s));
+    }
   }
   if (path == MOE_PATH_GEMV) {
     {
@@ -244,7 +254,8 @@ const char *moe_strerror(int code) {
 
 const char *moe_kernel_name(int kernel) {
   static const char *names[MOE_K_COUNT] = {"router_logits", "router_select", "permute",
-                                           "gate_up_swiglu", "down", "combine", "act_quant"};
+                                           "gate_up_swiglu", "down", "combine", "act_quant",
+                                           "route"};
   return (kernel >= 0 && kernel < MOE_K_COUNT) ? names[kernel] : "unknown";
 }
 
@@ -285,7 +296,8 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->inv, (size_t)Pm * 4},
       {(void **)&c->active, (size_t)E * 4},
       {(void **)&c->n_active, 16},
-      {(void **)&c->work_ctr, 16},
+      {(void **)&c->ticket, 16},
+      {(void **)&c->xnorm, (size_t)Tm * 4},
       {(void **)&c->tile_offsets, (size_t)(E + 1) * 4},
       {(void **)&c->hmax, (size_t)Pm * 4},
       {(void **)&c->x16, (size_t)(Tm * H) * 2},

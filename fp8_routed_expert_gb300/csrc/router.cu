@@ -17,32 +17,338 @@
 // bits) and selected again.  This is the "cheap bound first, exact work only
 // where the bound reaches the best score" pattern of Trochilus's output head
 // ("What makes it different").
+#include <climits>
+
 #include "common.cuh"
 #include "kernels.h"
+#include "permute.cuh"
 
 namespace fp8moe {
 
-// ------------------------------------------------------------------ logits, T small
-// One CTA of 8 warps per expert row; warp w owns the column slice
-// [w H/8, (w+1) H/8) and lane l the 4 columns 4 l + 128 j of that slice.  A
-// lane sums its products sequentially with fma, a 5-level butterfly adds the
-// 32 lanes, and one thread adds the 8 warp sums in order.  Rounding chain
-// length: 4 ceil(H/1024) + 5 + 8 (+1 for the bias, added in the select
-// kernel).  Also writes ||W_e||_2.
+// ------------------------------------------------------------------ selection
+struct SelectArgs {
+  const __nv_bfloat16 *x;
+  int64_t T;
+  const float *W, *bias;
+  int64_t E, H;
+  int k;
+  const float *logits;  // ks planes [ks][T][E] of partial logits
+  int ks;
+  const float *wnorm;   // ||W_e||_2
+  float gamma;          // gamma_d of the logit kernel's rounding chain
+  int32_t *idx;
+  float *wts;
+  int *err;
+};
+
+// Argmax over the experts a lane owns (e = lane + 32 j) that are not yet taken,
+// then over the warp: larger key first, lower expert on equal keys.
+template <typename K, typename F>
+__device__ __forceinline__ int warp_argmax(int E, uint32_t taken, F key, K *best_key) {
+  const int lane = threadIdx.x & 31;
+  K bk = K(0);
+  int be = -1;
+  for (int j = 0; lane + 32 * j < E; ++j) {
+    if (taken >> j & 1u) continue;
+    const int e = lane + 32 * j;
+    const K v = key(e);
+    if (be < 0 || v > bk) { bk = v; be = e; }  // ascending e: first max wins
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    K ok = __shfl_xor_sync(0xffffffffu, bk, o);
+    int oe = __shfl_xor_sync(0xffffffffu, be, o);
+    bool take = (oe >= 0) && (be < 0 || ok > bk || (ok == bk && oe < be));
+    if (take) { bk = ok; be = oe; }
+  }
+  *best_key = bk;
+  return be;
+}
+
+// ||x_t||_2 and max |x_t| by one warp (4 independent partial sums per lane
+// keep several loads in flight).
+__device__ __forceinline__ void x_stats(const __nv_bfloat16 *xt, int64_t H, float *norm, float *amax) {
+  const int lane = threadIdx.x & 31;
+  float ss = 0.f, am = 0.f;
+#pragma unroll 4
+  for (int64_t h = 4 * lane; h < H; h += 128) {
+    const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(xt + h));
+    const float v0 = bf16_bits_to_float(xv.x & 0xffffu), v1 = bf16_bits_to_float(xv.x >> 16);
+    const float v2 = bf16_bits_to_float(xv.y & 0xffffu), v3 = bf16_bits_to_float(xv.y >> 16);
+    ss = fmaf(v0, v0, ss); ss = fmaf(v1, v1, ss); ss = fmaf(v2, v2, ss); ss = fmaf(v3, v3, ss);
+    am = fmaxf(am, fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
+  }
+  *norm = sqrtf(warp_sum(ss));
+  *amax = warp_max(am);
+}
+
+// f16 copy of x_t for the tensor-core GEMV, scaled by an exact power of two
+// so that the largest magnitude fits f16's range; xscale[t] undoes it.
+__device__ __forceinline__ void x_to_f16(const __nv_bfloat16 *xt, int64_t H, float amax,
+                                         __half *x16t, float *xscale_t) {
+  const int lane = threadIdx.x & 31;
+  const int sh = f16_range_shift(amax);
+  const float down = exp2i(-sh);
+#pragma unroll 4
+  for (int64_t h = 4 * lane; h < H; h += 128) {
+    const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(xt + h));
+    uint2 o;
+    o.x = pack_f16x2(bf16_bits_to_float(xv.x & 0xffffu) * down, bf16_bits_to_float(xv.x >> 16) * down);
+    o.y = pack_f16x2(bf16_bits_to_float(xv.y & 0xffffu) * down, bf16_bits_to_float(xv.y >> 16) * down);
+    *reinterpret_cast<uint2 *>(x16t + h) = o;
+  }
+  if (lane == 0) *xscale_t = exp2i(sh);
+}
+
+// logit of expert e for x_t in f64 from exact products (bf16 x f32 fits in 53
+// bits), by the whole warp; four loads per lane in flight.
+__device__ __forceinline__ double exact_logit(const SelectArgs &a, const __nv_bfloat16 *xt, int e) {
+  const int lane = threadIdx.x & 31;
+  const float *w = a.W + (int64_t)e * a.H;
+  double acc = 0.0;
+  for (int64_t h0 = 4 * lane; h0 < a.H; h0 += 512) {
+    float4 wv[4];
+    uint2 xv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t h = h0 + 128 * u;
+      wv[u] = h < a.H ? __ldg(reinterpret_cast<const float4 *>(w + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      xv[u] = h < a.H ? __ldg(reinterpret_cast<const uint2 *>(xt + h)) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc = fma((double)bf16_bits_to_float(xv[u].x & 0xffffu), (double)wv[u].x, acc);
+      acc = fma((double)bf16_bits_to_float(xv[u].x >> 16), (double)wv[u].y, acc);
+      acc = fma((double)bf16_bits_to_float(xv[u].y & 0xffffu), (double)wv[u].z, acc);
+      acc = fma((double)bf16_bits_to_float(xv[u].y >> 16), (double)wv[u].w, acc);
+    }
+  }
+  double v = warp_sum(acc);
+  if (a.bias != nullptr) v += (double)a.bias[e];
+  return v;
+}
+
+// Top-k of token t by one warp.  Per-warp shared memory: lg and bt (E floats
+// each: logits + bias and their error bounds) and lg64 (E doubles).  Logits
+// are read with ld.global.cg so that planes written by other CTAs of the same
+// grid are seen.
+__device__ void select_token(const SelectArgs &a, int64_t t, float xn, float *lg, float *bt,
+                             double *lg64) {
+  const int lane = threadIdx.x & 31;
+  const int E = (int)a.E, k = a.k;
+  const __nv_bfloat16 *xt = a.x + t * a.H;
+
+  const float tiny = (float)a.H * 1.0e-37f;
+  bool finite = true;
+#pragma unroll 4
+  for (int e = lane; e < E; e += 32) {
+    float v = __ldcg(a.logits + t * a.E + e);
+    for (int z = 1; z < a.ks; ++z) v += __ldcg(a.logits + (z * a.T + t) * a.E + e);
+    float b = a.gamma * xn * __ldcg(a.wnorm + e) * 1.01f + tiny;
+    if (a.bias != nullptr) {
+      const float bb = a.bias[e];
+      v += bb;
+      b += fabsf(bb) * 1.2e-7f;
+    }
+    finite = finite && isfinite(v);
+    lg[e] = v;
+    bt[e] = b;
+  }
+  if (!__all_sync(0xffffffffu, finite) && lane == 0) set_error(a.err, DEV_ERR_NONFINITE);
+  __syncwarp();
+  auto beta = [&](int e) -> float { return bt[e]; };
+  auto key32 = [&](int e) -> float {
+    const float v = lg[e];
+    return isfinite(v) ? v : -INFINITY;
+  };
+
+  // f32 selection of the top k
+  uint32_t taken = 0;
+  int sel_e = -1;  // lane r holds the expert of rank r
+  float sel_v = 0.f;
+  for (int r = 0; r < k; ++r) {
+    float bv;
+    const int be = warp_argmax<float>(E, taken, key32, &bv);
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == r) { sel_e = be; sel_v = bv; }
+  }
+  // certify: every selected lower bound above every other upper bound, and
+  // adjacent selected experts separated by their bounds
+  float upper_rest = -INFINITY;
+  for (int j = 0; lane + 32 * j < E; ++j) {
+    if (taken >> j & 1u) continue;
+    const int e = lane + 32 * j;
+    upper_rest = fmaxf(upper_rest, key32(e) + beta(e));
+  }
+  upper_rest = warp_max(upper_rest);
+  const float lo_sel = (lane < k) ? sel_v - beta(sel_e) : INFINITY;
+  const float hi_next = __shfl_down_sync(0xffffffffu, (lane < k) ? sel_v + beta(sel_e) : -INFINITY, 1);
+  const bool ordered = (lane + 1 >= k) || (lo_sel > hi_next);
+  const float min_lo = -warp_max(-lo_sel);
+  const bool certified = __all_sync(0xffffffffu, ordered) && (k == E || min_lo > upper_rest) &&
+                         isfinite(min_lo);
+
+  if (certified) {
+    const float l0 = __shfl_sync(0xffffffffu, sel_v, 0);
+    const float ex = (lane < k) ? __expf(sel_v - l0) : 0.f;
+    const float z = warp_sum(ex);
+    if (lane < k) {
+      a.idx[t * k + lane] = sel_e;
+      a.wts[t * k + lane] = ex / z;
+    }
+    return;
+  }
+
+  // Refinement.  Candidates: every expert whose upper bound reaches the k-th
+  // largest lower bound (the others are certainly below k experts).  A
+  // candidate whose interval [l - beta, l + beta] overlaps no other
+  // candidate's is "isolated": its f32 value already orders it correctly
+  // against every candidate.  Only the others are recomputed in f64 from exact
+  // products; the top k is then taken on key = f64 value (recomputed) or f32
+  // value (isolated), which orders every pair of candidates exactly.
+  uint32_t taken2 = 0;
+  float kth_lo = -INFINITY;
+  auto lo_key = [&](int e) -> float { return key32(e) - beta(e); };
+  for (int r = 0; r < k; ++r) {
+    float bv;
+    const int be = warp_argmax<float>(E, taken2, lo_key, &bv);
+    if ((be & 31) == lane) taken2 |= 1u << (be >> 5);
+    kth_lo = bv;
+  }
+  uint32_t cmask = 0;
+  for (int j = 0; lane + 32 * j < E; ++j) {
+    const int e = lane + 32 * j;
+    if (!(key32(e) + beta(e) < kth_lo) && isfinite(lg[e])) cmask |= 1u << j;
+  }
+  // compact the candidates to one per lane (at most 32; more only in
+  // degenerate near-total ties, where every candidate is recomputed)
+  const int ccount = __popc(cmask);
+  int cpre = ccount;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, cpre, o);
+    if (lane >= o) cpre += n;
+  }
+  const int ctotal = __shfl_sync(0xffffffffu, cpre, 31);
+  cpre -= ccount;
+  int *cand = reinterpret_cast<int *>(lg64);  // first 32 slots; lg64 is rewritten below
+  const bool compact = ctotal <= 32;
+  double key = -INFINITY;
+  int my_e = -1;
+  if (compact) {
+    {
+      uint32_t m = cmask;
+      int slot = cpre;
+      while (m != 0u) {
+        const int j = __ffs(m) - 1;
+        m &= m - 1u;
+        cand[slot++] = lane + 32 * j;
+      }
+    }
+    __syncwarp();
+    my_e = lane < ctotal ? cand[lane] : -1;
+    __syncwarp();
+    const float mv = my_e >= 0 ? lg[my_e] : 0.f, mb = my_e >= 0 ? bt[my_e] : 0.f;
+    const float mlo = mv - mb, mup = mv + mb;
+    bool isolated = true;
+    for (int s2 = 0; s2 < ctotal; ++s2) {
+      const float olo = __shfl_sync(0xffffffffu, mlo, s2), oup = __shfl_sync(0xffffffffu, mup, s2);
+      if (s2 != lane && mlo <= oup && olo <= mup) isolated = false;
+    }
+    uint32_t rmask = __ballot_sync(0xffffffffu, my_e >= 0 && !isolated);
+    key = my_e >= 0 ? (double)mv : -INFINITY;
+    while (rmask != 0u) {
+      const int src = __ffs(rmask) - 1;
+      rmask &= rmask - 1u;
+      const int e = __shfl_sync(0xffffffffu, my_e, src);
+      const double v = exact_logit(a, xt, e);
+      if (lane == src) key = v;
+    }
+  } else {
+    for (int j = 0; lane + 32 * j < E; ++j) lg64[lane + 32 * j] = -INFINITY;
+    __syncwarp();
+    for (int src = 0; src < 32; ++src) {
+      uint32_t m = __shfl_sync(0xffffffffu, cmask, src);
+      while (m != 0u) {
+        const int j = __ffs(m) - 1;
+        m &= m - 1u;
+        const int e = src + 32 * j;
+        const double v = exact_logit(a, xt, e);
+        if (lane == 0) lg64[e] = v;
+      }
+    }
+    __syncwarp();
+  }
+
+  // top k on the keys, larger first, lower expert on equal keys
+  int fe = -1;
+  double fv = 0.0;
+  if (compact) {
+    bool used = my_e < 0;
+    for (int r = 0; r < k; ++r) {
+      double bk = used ? -INFINITY : key;
+      int be = used ? INT_MAX : my_e;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const double ok = __shfl_xor_sync(0xffffffffu, bk, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ok > bk || (ok == bk && oe < be)) { bk = ok; be = oe; }
+      }
+      if (be == my_e) used = true;
+      if (lane == r) { fe = be; fv = bk; }
+    }
+  } else {
+    auto key64 = [&](int e) -> double { return lg64[e]; };
+    uint32_t taken3 = 0;
+    for (int r = 0; r < k; ++r) {
+      double bv;
+      const int be = warp_argmax<double>(E, taken3, key64, &bv);
+      if ((be & 31) == lane) taken3 |= 1u << (be >> 5);
+      if (lane == r) { fe = be; fv = bv; }
+    }
+  }
+  const double l0 = __shfl_sync(0xffffffffu, fv, 0);
+  const double ex = (lane < k) ? exp(fv - l0) : 0.0;
+  const double z = warp_sum(ex);
+  if (lane < k) {
+    if (fe < 0 || fe >= E) { set_error(a.err, DEV_ERR_BOUNDS); fe = 0; }
+    a.idx[t * k + lane] = fe;
+    a.wts[t * k + lane] = (float)(ex / z);
+  }
+}
+
+// ------------------------------------------------------------------ fused small-batch routing
+// One launch for T <= 64.  CTA e computes the logits of expert e for every
+// token (8 warps split H: lane chain 4 ceil(H/1024), butterfly 5, warp sum 8,
+// +1 bias) and ||W_e||; the same pass gives every CTA ||x_t|| and max |x_t|,
+// and CTA c % E writes 128-column chunk c of the f16 copy of x.  The last CTA
+// to finish (an atomic ticket, reset for the next call) selects the top k of
+// every token and sorts the pairs by expert.
+constexpr int kRouteWarps = 8;
+
 template <int TG>
-__global__ void __launch_bounds__(256) router_logits_split_kernel(
-    const __nv_bfloat16 *__restrict__ x, int64_t T, const float *__restrict__ W, int64_t E,
-    int64_t H, float *__restrict__ logits, float *__restrict__ wnorm) {
-  __shared__ float part[8][TG];
-  __shared__ float ssq[8];
+__global__ void __launch_bounds__(32 * kRouteWarps) route_decode_kernel(
+    SelectArgs a, float *__restrict__ logits_w, float *__restrict__ wnorm_w,
+    float *__restrict__ xnorm, __half *__restrict__ x16, float *__restrict__ xscale,
+    int32_t *__restrict__ ticket, int tile_m, SortOut so, uint32_t *__restrict__ pos_max) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ float part[kRouteWarps][TG], part_ss[kRouteWarps][TG], part_am[kRouteWarps][TG];
+  __shared__ float ssq[kRouteWarps];
+  __shared__ float s_am[kRouterWarpMaxT];
+  __shared__ int s_last;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t E = a.E, H = a.H, T = a.T;
   const int64_t e = blockIdx.x;
-  const int64_t slice = H / 8;
+  pdl_trigger();  // the next kernel may be scheduled; it waits for this one to finish
+
+  // ---- phase A: logits of expert e, ||W_e||, and (redundantly in every CTA,
+  // from the same pass over x) ||x_t|| and max |x_t|
+  const int64_t slice = H / kRouteWarps;
   const int64_t h_lo = wid * slice, h_hi = h_lo + slice;
-  const float *w = W + e * H;
+  const float *w = a.W + e * H;
   float ss = 0.f;
-  for (int64_t h = h_lo + 4 * lane; h < h_hi; h += 128) {
-    float4 wv = __ldg(reinterpret_cast<const float4 *>(w + h));
+  for (int64_t hh = h_lo + 4 * lane; hh < h_hi; hh += 128) {
+    const float4 wv = __ldg(reinterpret_cast<const float4 *>(w + hh));
     ss = fmaf(wv.x, wv.x, ss);
     ss = fmaf(wv.y, wv.y, ss);
     ss = fmaf(wv.z, wv.z, ss);
@@ -50,44 +356,120 @@ __global__ void __launch_bounds__(256) router_logits_split_kernel(
   }
   ss = warp_sum(ss);
   if (lane == 0) ssq[wid] = ss;
-
   for (int64_t t0 = 0; t0 < T; t0 += TG) {
-    float acc[TG];
+    float acc[TG], xs[TG], xm[TG];
 #pragma unroll
-    for (int j = 0; j < TG; ++j) acc[j] = 0.f;
-    for (int64_t h = h_lo + 4 * lane; h < h_hi; h += 128) {
-      const float4 wv = __ldg(reinterpret_cast<const float4 *>(w + h));
+    for (int j = 0; j < TG; ++j) { acc[j] = 0.f; xs[j] = 0.f; xm[j] = 0.f; }
+    for (int64_t hh = h_lo + 4 * lane; hh < h_hi; hh += 128) {
+      const float4 wv = __ldg(reinterpret_cast<const float4 *>(w + hh));
 #pragma unroll
       for (int j = 0; j < TG; ++j) {
         if (t0 + j < T) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(x + (t0 + j) * H + h));
-          acc[j] = fmaf(bf16_bits_to_float(xv.x & 0xffffu), wv.x, acc[j]);
-          acc[j] = fmaf(bf16_bits_to_float(xv.x >> 16), wv.y, acc[j]);
-          acc[j] = fmaf(bf16_bits_to_float(xv.y & 0xffffu), wv.z, acc[j]);
-          acc[j] = fmaf(bf16_bits_to_float(xv.y >> 16), wv.w, acc[j]);
+          const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(a.x + (t0 + j) * H + hh));
+          const float v0 = bf16_bits_to_float(xv.x & 0xffffu), v1 = bf16_bits_to_float(xv.x >> 16);
+          const float v2 = bf16_bits_to_float(xv.y & 0xffffu), v3 = bf16_bits_to_float(xv.y >> 16);
+          acc[j] = fmaf(v0, wv.x, acc[j]);
+          acc[j] = fmaf(v1, wv.y, acc[j]);
+          acc[j] = fmaf(v2, wv.z, acc[j]);
+          acc[j] = fmaf(v3, wv.w, acc[j]);
+          xs[j] = fmaf(v0, v0, xs[j]); xs[j] = fmaf(v1, v1, xs[j]);
+          xs[j] = fmaf(v2, v2, xs[j]); xs[j] = fmaf(v3, v3, xs[j]);
+          xm[j] = fmaxf(xm[j], fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
         }
       }
     }
 #pragma unroll
     for (int j = 0; j < TG; ++j) {
-      const float s = warp_sum(acc[j]);
-      if (lane == 0) part[wid][j] = s;
+      const float s = warp_sum(acc[j]), q2 = warp_sum(xs[j]), m = warp_max(xm[j]);
+      if (lane == 0) { part[wid][j] = s; part_ss[wid][j] = q2; part_am[wid][j] = m; }
     }
     __syncthreads();
     if (threadIdx.x < TG && t0 + threadIdx.x < T) {
-      float v = 0.f;
+      float v = 0.f, q2 = 0.f, m = 0.f;
 #pragma unroll
-      for (int q = 0; q < 8; ++q) v += part[q][threadIdx.x];
-      logits[(t0 + threadIdx.x) * E + e] = v;
-    }
-    if (t0 == 0 && threadIdx.x == 32) {
-      float v = 0.f;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) v += ssq[q];
-      wnorm[e] = sqrtf(v);
+      for (int q = 0; q < kRouteWarps; ++q) {
+        v += part[q][threadIdx.x];
+        q2 += part_ss[q][threadIdx.x];
+        m = fmaxf(m, part_am[q][threadIdx.x]);
+      }
+      const int64_t t = t0 + threadIdx.x;
+      logits_w[t * E + e] = v;
+      s_am[t] = m;
+      if (e == 0) {
+        xnorm[t] = sqrtf(q2);
+        if (xscale != nullptr) xscale[t] = exp2i(f16_range_shift(m));
+      }
     }
     __syncthreads();
   }
+  if (threadIdx.x == 32) {
+    float v = 0.f;
+#pragma unroll
+    for (int q = 0; q < kRouteWarps; ++q) v += ssq[q];
+    wnorm_w[e] = sqrtf(v);
+  }
+  // f16 copy of x: 128-column chunk c of every token is written by CTA c % E,
+  // scaled by the token's exact power of two (max |x_t| known from the pass)
+  if (x16 != nullptr) {
+    const int64_t nch = H / 128;
+    for (int64_t c = e; c < nch; c += E) {
+      for (int64_t t = wid; t < T; t += kRouteWarps) {
+        const float down = exp2i(-f16_range_shift(s_am[t]));
+        const int64_t h = c * 128 + 4 * lane;
+        const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(a.x + t * H + h));
+        uint2 o;
+        o.x = pack_f16x2(bf16_bits_to_float(xv.x & 0xffffu) * down, bf16_bits_to_float(xv.x >> 16) * down);
+        o.y = pack_f16x2(bf16_bits_to_float(xv.y & 0xffffu) * down, bf16_bits_to_float(xv.y >> 16) * down);
+        *reinterpret_cast<uint2 *>(x16 + t * H + h) = o;
+      }
+    }
+  }
+
+  // ---- ticket: the last CTA continues
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(ticket, 1) == (int)gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- phase B: selection (warp per token), then the stable sort
+  double *lg64 = reinterpret_cast<double *>(smem_raw) + (size_t)wid * E;
+  float *lg = reinterpret_cast<float *>(smem_raw + (size_t)kRouteWarps * E * sizeof(double)) + (size_t)wid * 2 * E;
+  for (int64_t t = wid; t < T; t += kRouteWarps) select_token(a, t, __ldcg(xnorm + t), lg, lg + E, lg64);
+  if (pos_max != nullptr)
+    for (int64_t p = threadIdx.x; p < T * a.k; p += blockDim.x) pos_max[p] = 0u;
+  __threadfence_block();
+  __syncthreads();
+  cta_counting_sort<kRouteWarps>(a.idx, T * a.k, (int)E, tile_m, so, reinterpret_cast<int *>(smem_raw), a.err);
+  if (threadIdx.x == 0) *ticket = 0;
+}
+
+// f16 copies of every token (the GEMV path above the fused-routing size).
+__global__ void __launch_bounds__(128) x_to_f16_kernel(const __nv_bfloat16 *__restrict__ x, int64_t T,
+                                                       int64_t H, __half *__restrict__ x16,
+                                                       float *__restrict__ xscale) {
+  const int64_t t = (int64_t)blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float xn, amax;
+  x_stats(x + t * H, H, &xn, &amax);
+  x_to_f16(x + t * H, H, amax, x16 + t * H, xscale + t);
+}
+
+// ------------------------------------------------------------------ selection, T large
+// One warp per token.  Shared memory per warp: E floats and E doubles.
+__global__ void __launch_bounds__(128) router_select_kernel(SelectArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int64_t t = (int64_t)blockIdx.x * nw + wid;
+  double *lg64 = reinterpret_cast<double *>(smem_raw) + (size_t)wid * a.E;
+  float *lg = reinterpret_cast<float *>(smem_raw + (size_t)nw * a.E * sizeof(double)) + (size_t)wid * 2 * a.E;
+  if (t >= a.T) return;
+  float xn, amax;
+  x_stats(a.x + t * a.H, a.H, &xn, &amax);
+  select_token(a, t, xn, lg, lg + a.E, lg64);
 }
 
 // ------------------------------------------------------------------ logits, T large
@@ -200,198 +582,6 @@ __global__ void __launch_bounds__(128) row_norm_kernel(const float *__restrict__
   if (lane == 0) wnorm[e] = sqrtf(ss);
 }
 
-// ------------------------------------------------------------------ selection
-// Argmax over the experts a lane owns (e = lane + 32 j) that are not yet taken,
-// then over the warp: larger key first, lower expert on equal keys.
-template <typename K, typename F>
-__device__ __forceinline__ int warp_argmax(int E, uint32_t taken, F key, K *best_key) {
-  const int lane = threadIdx.x & 31;
-  K bk = K(0);
-  int be = -1;
-  for (int j = 0; lane + 32 * j < E; ++j) {
-    if (taken >> j & 1u) continue;
-    const int e = lane + 32 * j;
-    const K v = key(e);
-    if (be < 0 || v > bk) { bk = v; be = e; }  // ascending e: first max wins
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    K ok = __shfl_xor_sync(0xffffffffu, bk, o);
-    int oe = __shfl_xor_sync(0xffffffffu, be, o);
-    bool take = (oe >= 0) && (be < 0 || ok > bk || (ok == bk && oe < be));
-    if (take) { bk = ok; be = oe; }
-  }
-  *best_key = bk;
-  return be;
-}
-
-// One warp per token.  Shared memory per warp: E floats (logits + bias) and
-// E doubles (refined logits).
-__global__ void __launch_bounds__(128) router_select_kernel(
-    const __nv_bfloat16 *__restrict__ x, int64_t T, const float *__restrict__ W,
-    const float *__restrict__ bias, int64_t E, int64_t H, int k, const float *__restrict__ logits,
-    const float *__restrict__ wnorm, int ks, float gamma_d, int32_t *__restrict__ idx,
-    float *__restrict__ wts, __half *__restrict__ x16, float *__restrict__ xscale,
-    int *__restrict__ err) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int nw = blockDim.x >> 5;
-  const int64_t t = (int64_t)blockIdx.x * nw + wid;
-  double *lg64 = reinterpret_cast<double *>(smem_raw) + (size_t)wid * E;
-  float *lg = reinterpret_cast<float *>(smem_raw + (size_t)nw * E * sizeof(double)) + (size_t)wid * E;
-  if (t >= T) return;
-  const __nv_bfloat16 *xt = x + t * H;
-
-  // ||x_t||_2 and max |x_t|
-  float ss = 0.f, amax = 0.f;
-  for (int64_t h = 4 * lane; h < H; h += 128) {
-    uint2 xv = __ldg(reinterpret_cast<const uint2 *>(xt + h));
-    float v0 = bf16_bits_to_float(xv.x & 0xffffu), v1 = bf16_bits_to_float(xv.x >> 16);
-    float v2 = bf16_bits_to_float(xv.y & 0xffffu), v3 = bf16_bits_to_float(xv.y >> 16);
-    ss = fmaf(v0, v0, ss); ss = fmaf(v1, v1, ss); ss = fmaf(v2, v2, ss); ss = fmaf(v3, v3, ss);
-    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
-  }
-  const float xn = sqrtf(warp_sum(ss));
-  amax = warp_max(amax);
-
-  // f16 copy of x_t for the tensor-core GEMV, scaled by an exact power of two
-  // so that the largest magnitude fits f16's range.
-  if (x16 != nullptr) {
-    const int sh = f16_range_shift(amax);
-    const float down = exp2i(-sh);
-    for (int64_t h = 4 * lane; h < H; h += 128) {
-      uint2 xv = __ldg(reinterpret_cast<const uint2 *>(xt + h));
-      uint2 o;
-      o.x = pack_f16x2(bf16_bits_to_float(xv.x & 0xffffu) * down, bf16_bits_to_float(xv.x >> 16) * down);
-      o.y = pack_f16x2(bf16_bits_to_float(xv.y & 0xffffu) * down, bf16_bits_to_float(xv.y >> 16) * down);
-      *reinterpret_cast<uint2 *>(x16 + t * H + h) = o;
-    }
-    if (lane == 0) xscale[t] = exp2i(sh);
-  }
-
-  // f32 logits (+ bias) into shared memory
-  bool finite = true;
-  for (int e = lane; e < E; e += 32) {
-    float v = logits[t * E + e];
-    for (int z = 1; z < ks; ++z) v += logits[(z * T + t) * E + e];
-    if (bias != nullptr) v += bias[e];
-    finite = finite && isfinite(v);
-    lg[e] = v;
-  }
-  if (!__all_sync(0xffffffffu, finite)) {
-    if (lane == 0) set_error(err, DEV_ERR_NONFINITE);
-    // still produce a valid routing: map non-finite logits to -inf below
-  }
-  __syncwarp();
-  const float tiny = (float)H * 1.0e-37f;
-  auto beta = [&](int e) -> float {
-    float b = gamma_d * xn * wnorm[e] * 1.01f + tiny;
-    if (bias != nullptr) b += fabsf(bias[e]) * 1.2e-7f;
-    return b;
-  };
-  auto key32 = [&](int e) -> float {
-    float v = lg[e];
-    return isfinite(v) ? v : -INFINITY;
-  };
-
-  // f32 selection of the top k
-  uint32_t taken = 0;
-  int sel_e = -1;      // lane r holds the expert of rank r
-  float sel_v = 0.f;
-  for (int r = 0; r < k; ++r) {
-    float bv;
-    int be = warp_argmax<float>((int)E, taken, key32, &bv);
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
-    if (lane == r) { sel_e = be; sel_v = bv; }
-  }
-  // certify: every selected lower bound above every other upper bound, and
-  // adjacent selected experts separated by their bounds
-  float upper_rest = -INFINITY;
-  for (int j = 0; lane + 32 * j < E; ++j) {
-    if (taken >> j & 1u) continue;
-    const int e = lane + 32 * j;
-    upper_rest = fmaxf(upper_rest, key32(e) + beta(e));
-  }
-  upper_rest = warp_max(upper_rest);
-  float lo_sel = (lane < k) ? sel_v - beta(sel_e) : INFINITY;
-  float hi_next = __shfl_down_sync(0xffffffffu, (lane < k) ? sel_v + beta(sel_e) : -INFINITY, 1);
-  bool ordered = (lane + 1 >= k) || (lo_sel > hi_next);
-  float min_lo = -warp_max(-lo_sel);
-  bool certified = __all_sync(0xffffffffu, ordered) && (k == E || min_lo > upper_rest) &&
-                   isfinite(min_lo);
-
-  if (certified) {
-    const float l0 = __shfl_sync(0xffffffffu, sel_v, 0);
-    float ex = (lane < k) ? __expf(sel_v - l0) : 0.f;
-    float z = warp_sum(ex);
-    if (lane < k) {
-      idx[t * k + lane] = sel_e;
-      wts[t * k + lane] = ex / z;
-    }
-    return;
-  }
-
-  // Refinement: the k-th largest lower bound; every expert whose upper bound
-  // reaches it is a candidate and is recomputed in f64.
-  uint32_t taken2 = 0;
-  float kth_lo = -INFINITY;
-  auto lo_key = [&](int e) -> float { return key32(e) - beta(e); };
-  for (int r = 0; r < k; ++r) {
-    float bv;
-    int be = warp_argmax<float>((int)E, taken2, lo_key, &bv);
-    if ((be & 31) == lane) taken2 |= 1u << (be >> 5);
-    kth_lo = bv;
-  }
-  // candidates: each lane tests its own experts; the warp then recomputes
-  // them one at a time (lane order, then j), all lanes cooperating on the dot
-  uint32_t cmask = 0;
-  for (int j = 0; lane + 32 * j < E; ++j) {
-    const int e = lane + 32 * j;
-    if (!(key32(e) + beta(e) < kth_lo) && isfinite(lg[e])) cmask |= 1u << j;
-    else lg64[e] = -INFINITY;
-  }
-  for (int src = 0; src < 32; ++src) {
-    uint32_t m = __shfl_sync(0xffffffffu, cmask, src);
-    while (m != 0u) {
-      const int j = __ffs(m) - 1;
-      m &= m - 1u;
-      const int e = src + 32 * j;
-      const float *w = W + (int64_t)e * H;
-      double acc = 0.0;
-      for (int64_t h = 4 * lane; h < H; h += 128) {
-        float4 wv = __ldg(reinterpret_cast<const float4 *>(w + h));
-        uint2 xv = __ldg(reinterpret_cast<const uint2 *>(xt + h));
-        acc = fma((double)bf16_bits_to_float(xv.x & 0xffffu), (double)wv.x, acc);
-        acc = fma((double)bf16_bits_to_float(xv.x >> 16), (double)wv.y, acc);
-        acc = fma((double)bf16_bits_to_float(xv.y & 0xffffu), (double)wv.z, acc);
-        acc = fma((double)bf16_bits_to_float(xv.y >> 16), (double)wv.w, acc);
-      }
-      double v = warp_sum(acc);
-      if (bias != nullptr) v += (double)bias[e];
-      if (lane == 0) lg64[e] = v;
-    }
-  }
-  __syncwarp();
-  auto key64 = [&](int e) -> double { return lg64[e]; };
-  uint32_t taken3 = 0;
-  int fe = -1;
-  double fv = 0.0;
-  for (int r = 0; r < k; ++r) {
-    double bv;
-    int be = warp_argmax<double>((int)E, taken3, key64, &bv);
-    if ((be & 31) == lane) taken3 |= 1u << (be >> 5);
-    if (lane == r) { fe = be; fv = bv; }
-  }
-  const double l0 = __shfl_sync(0xffffffffu, fv, 0);
-  double ex = (lane < k) ? exp(fv - l0) : 0.0;
-  double z = warp_sum(ex);
-  if (lane < k) {
-    if (fe < 0 || fe >= E) { set_error(err, DEV_ERR_BOUNDS); fe = 0; }
-    idx[t * k + lane] = fe;
-    wts[t * k + lane] = (float)(ex / z);
-  }
-}
-
 // ------------------------------------------------------------------ launchers
 
 int router_k_split(int64_t T, int64_t E, int64_t H, int sms) {
@@ -409,36 +599,73 @@ int router_chain_depth(int64_t T, int64_t H, int ks) {
                               : (int)(128 + H / 128 + ks + 1);
 }
 
-cudaError_t launch_router_logits(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
-                                 int64_t H, int ks, float *logits, float *wnorm, cudaStream_t s) {
-  if (T <= kRouterWarpMaxT) {
-    if (T <= 1)
-      router_logits_split_kernel<1><<<(unsigned)E, 256, 0, s>>>(x, T, W, E, H, logits, wnorm);
-    else
-      router_logits_split_kernel<8><<<(unsigned)E, 256, 0, s>>>(x, T, W, E, H, logits, wnorm);
-    return cudaGetLastError();
+static SelectArgs select_args(const __nv_bfloat16 *x, int64_t T, const float *W, const float *bias,
+                              int64_t E, int64_t H, int k, const float *logits, int ks,
+                              const float *wnorm, float gamma, int32_t *idx, float *wts, int *err) {
+  SelectArgs a;
+  a.x = x; a.T = T; a.W = W; a.bias = bias; a.E = E; a.H = H; a.k = k;
+  a.logits = logits; a.ks = ks; a.wnorm = wnorm; a.gamma = gamma;
+  a.idx = idx; a.wts = wts; a.err = err;
+  return a;
+}
+
+size_t route_decode_smem(int64_t E) {
+  const size_t sel = (size_t)kRouteWarps * E * (sizeof(double) + 2 * sizeof(float));
+  const size_t srt = cta_sort_smem(kRouteWarps, (int)E);
+  return sel > srt ? sel : srt;
+}
+
+cudaError_t launch_route_decode(const __nv_bfloat16 *x, int64_t T, const float *W, const float *bias,
+                                int64_t E, int64_t H, int k, float gamma, float *logits, float *wnorm,
+                                float *xnorm, __half *x16, float *xscale, int32_t *ticket,
+                                int32_t *idx, float *wts, int32_t *counts, int32_t *offsets,
+                                int32_t *perm, int32_t *inv, int32_t *active, int32_t *n_active,
+                                int32_t *tile_offsets, int tile_m, uint32_t *pos_max, int *err,
+                                cudaStream_t s) {
+  SelectArgs a = select_args(x, T, W, bias, E, H, k, logits, 1, wnorm, gamma, idx, wts, err);
+  SortOut so{counts, offsets, perm, inv, active, n_active, tile_offsets};
+  const size_t smem = route_decode_smem(E);
+  cudaError_t e;
+  if (T <= 1) {
+    auto kern = route_decode_kernel<1>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+    kern<<<(unsigned)E, 32 * kRouteWarps, smem, s>>>(a, logits, wnorm, xnorm, x16, xscale, ticket, tile_m, so, pos_max);
+  } else {
+    auto kern = route_decode_kernel<8>;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
+    kern<<<(unsigned)E, 32 * kRouteWarps, smem, s>>>(a, logits, wnorm, xnorm, x16, xscale, ticket, tile_m, so, pos_max);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_logits_tiled(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
+                                       int64_t H, int ks, float *logits, float *wnorm, cudaStream_t s) {
   row_norm_kernel<<<(unsigned)((E + 3) / 4), 128, 0, s>>>(W, E, H, wnorm);
   dim3 grid((unsigned)((E + 63) / 64), (unsigned)((T + 63) / 64), (unsigned)ks);
   router_logits_tiled_kernel<<<grid, 256, 0, s>>>(x, T, W, E, H, logits);
   return cudaGetLastError();
 }
 
-size_t router_select_smem(int64_t E) { return (size_t)4 * E * (sizeof(double) + sizeof(float)); }
+cudaError_t launch_x_to_f16(const __nv_bfloat16 *x, int64_t T, int64_t H, __half *x16, float *xscale,
+                           cudaStream_t s) {
+  x_to_f16_kernel<<<(unsigned)((T + 3) / 4), 128, 0, s>>>(x, T, H, x16, xscale);
+  return cudaGetLastError();
+}
+
+size_t router_select_smem(int64_t E) { return (size_t)4 * E * (sizeof(double) + 2 * sizeof(float)); }
 
 cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float *W,
                                  const float *bias, int64_t E, int64_t H, int k,
                                  const float *logits, const float *wnorm, int ks, float gamma_d,
-                                 int32_t *idx, float *wts, __half *x16, float *xscale, int *err,
-                                 cudaStream_t s) {
+                                 int32_t *idx, float *wts, int *err, cudaStream_t s) {
+  SelectArgs a = select_args(x, T, W, bias, E, H, k, logits, ks, wnorm, gamma_d, idx, wts, err);
   const size_t smem = router_select_smem(E);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(router_select_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  router_select_kernel<<<(unsigned)((T + 3) / 4), 128, smem, s>>>(
-      x, T, W, bias, E, H, k, logits, wnorm, ks, gamma_d, idx, wts, x16, xscale, err);
+  router_select_kernel<<<(unsigned)((T + 3) / 4), 128, smem, s>>>(a);
   return cudaGetLastError();
 }
 

@@ -13,7 +13,8 @@ from ._lib import C, MoEConfig, check, lib
 
 PATHS = {"auto": C["MOE_PATH_AUTO"], "gemv": C["MOE_PATH_GEMV"], "gemm": C["MOE_PATH_GEMM"]}
 KERNELS = {name: C[f"MOE_K_{name.upper()}"] for name in
-           ("router_logits", "router_select", "permute", "gate_up", "down", "combine", "act_quant")}
+           ("router_logits", "router_select", "permute", "gate_up", "down", "combine", "act_quant",
+            "route")}
 
 
 def _ptr(t: torch.Tensor | None) -> int | None:

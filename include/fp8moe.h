@@ -167,7 +167,8 @@ int moe_set_path(moe_ctx *ctx, int path);
 #define MOE_K_DOWN 4    /* grouped GEMV or GEMM for W2            */
 #define MOE_K_COMBINE 5
 #define MOE_K_ACT_QUANT 6
-#define MOE_K_COUNT 7
+#define MOE_K_ROUTE 7   /* small batches: logits, selection and sort in one kernel */
+#define MOE_K_COUNT 8
 int moe_set_timing(moe_ctx *ctx, int mask);
 int moe_kernel_time(moe_ctx *ctx, int kernel, double *total_ms, int64_t *launches);
 int64_t moe_launch_count(moe_ctx *ctx);

@@ -278,8 +278,8 @@ def test_kernel_timing_api():
     n0 = layer.launch_count()
     for _ in range(3):
         run(layer, x, dw, fam.top_k)
-    assert layer.launch_count() - n0 == 3 * 6
-    for name in ("router_logits", "router_select", "permute", "gate_up", "down", "combine"):
+    assert layer.launch_count() - n0 == 3 * 4   # fused routing, gate/up, down, combine
+    for name in ("route", "gate_up", "down", "combine"):
         ms, n = layer.kernel_time(name)
         assert n == 3 and ms > 0, name
     layer.set_timing(["gate_up"])
