@@ -39,6 +39,9 @@ constexpr int kTileM = 128;
 constexpr int kRouterMaxKSplit = 8;
 int router_k_split(int64_t T, int64_t E, int64_t H, int sms);
 int router_chain_depth(int64_t T, int64_t H, int ks);
+// gamma_d = d u / (1 - d u) of the logit kernel's longest rounding chain d,
+// rounded up: the relative factor of the router's error bound.
+float router_gamma(int64_t T, int64_t H, int ks);
 // T <= kRouterWarpMaxT: logits, selection and the pair sort in one launch
 // (ticket: an int32 that is 0 between calls).
 size_t route_decode_smem(int64_t E);

@@ -74,13 +74,6 @@ int check_config(const moe_config *c) {
   return MOE_OK;
 }
 
-float router_gamma(int64_t T, int64_t H, int ks) {
-  const double u = std::ldexp(1.0, -24);
-  const double d = (double)router_chain_depth(T, H, ks);
-  const double g = d * u / (1.0 - d * u);
-  return std::nextafter((float)(g * (1.0 + 1e-6)), INFINITY);
-}
-
 // Events around one kernel launch when timing is on.
 struct Timed {
   moe_ctx *c;

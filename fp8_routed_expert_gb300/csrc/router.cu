@@ -599,6 +599,13 @@ int router_chain_depth(int64_t T, int64_t H, int ks) {
                               : (int)(128 + H / 128 + ks + 1);
 }
 
+float router_gamma(int64_t T, int64_t H, int ks) {
+  const double u = 1.0 / 16777216.0;  // 2^-24
+  const double d = (double)router_chain_depth(T, H, ks);
+  const double g = d * u / (1.0 - d * u);
+  return nextafterf((float)(g * (1.0 + 1e-6)), INFINITY);
+}
+
 static SelectArgs select_args(const __nv_bfloat16 *x, int64_t T, const float *W, const float *bias,
                               int64_t E, int64_t H, int k, const float *logits, int ks,
                               const float *wnorm, float gamma, int32_t *idx, float *wts, int *err) {

@@ -184,6 +184,38 @@ const char *moe_kernel_name(int kernel);
 int moe_debug_copy(moe_ctx *ctx, const char *name, void *dst, int64_t capacity, int64_t *nbytes,
                    void *stream);
 
+/*
+ * moe_route_noalloc - the routing step alone (steps 1 and 2 above) for callers
+ * that may not allocate device memory once running: applications that hand
+ * all device memory to their own allocator at start-up, or inference loops
+ * with a fixed memory budget, where a cudaMalloc could fail or stall the
+ * device.  It allocates nothing and needs no context: its temporary buffers
+ * live in one statically sized device array of this library (about 269 KB,
+ * held on every GPU that loads the library until the process exits).
+ * There is no counterpart in the pages; it computes the same routing as
+ * moe_layer_forward followed by moe_get_routing.
+ *   hidden      : device, bf16 [T, H], 16-byte aligned; T <= 64.
+ *   H           : multiple of 128, <= 65536.
+ *   router_w    : device, f32 [E, H], 16-byte aligned; 1 <= E <= 1024.
+ *   router_bias : device, f32 [E], or NULL.
+ *   top_k       : 1..min(E, 32).
+ *   idx, wts    : device outputs, int32 / f32 [T, k], rank order.
+ *   counts      : device output, int32 [E].
+ *   offsets     : device output, int32 [E+1].
+ *   perm, inv   : device outputs, int32 [T*k].
+ *   stream      : cudaStream_t or NULL.
+ * Sizes beyond these limits return MOE_ERR_SHAPE; T = 0 is a no-op.  The
+ * first call on a device looks up the array's device address (a host-side
+ * query, done once per device, with that device current): make that first
+ * call outside any stream capture.  Every call shares the one array and
+ * clears the part that must start at zero; calls whose work overlaps on the
+ * GPU (other streams, other host threads) race on it and must be serialised
+ * by the caller.  Device-side errors (non-finite logits) are not reported.
+ */
+int moe_route_noalloc(const void *hidden, int64_t T, int64_t H, const float *router_w,
+                      const float *router_bias, int64_t E, int32_t top_k, int32_t *idx, float *wts,
+                      int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *inv, void *stream);
+
 #ifdef __cplusplus
 }
 #endif
