@@ -62,6 +62,22 @@ def dist_env():
         int(os.environ.get("WORLD_SIZE", 1))
 
 
+def reduce_max(values, device="cpu"):
+    """Element-wise maximum of per-rank floats over the process group (each
+    rank gets the result); identity without a process group."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_throughput(world: int, tokens_per_rank: int, max_ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch per step, and the
+    job's step lasts as long as the slowest rank's."""
+    return world * tokens_per_rank / (max_ms_per_step / 1e3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -277,10 +293,7 @@ def run_native(args, rank, local_rank, world):
         e2e_ms.append(a.elapsed_time(b))
     e2e_step = sum(e2e_ms) / K2
 
-    stats = torch.tensor([step_ms, e2e_step], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(stats, op=torch.distributed.ReduceOp.MAX)
-    step_ms, e2e_step = stats.tolist()
+    step_ms, e2e_step = reduce_max([step_ms, e2e_step], device=dev)
     if rank != 0:
         return None
 
@@ -307,7 +320,7 @@ def run_native(args, rank, local_rank, world):
     layer_bytes = sb["w13"] + sb["w2"] + sb["router"] + 2 * T * fam.hidden * 2
     layer_gbs = layer_bytes / (step_ms / 1e3) / 1e9
     expert_flops = 6.0 * P * fam.hidden * fam.inter
-    value = world * T / (step_ms / 1e3)
+    value = job_throughput(world, T, step_ms)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
@@ -324,7 +337,7 @@ def run_native(args, rank, local_rank, world):
         "layer": {"bytes": layer_bytes, "gbs": layer_gbs, "hbm_frac": layer_gbs / hbm,
                   "expert_tflops": expert_flops / (step_ms / 1e3) / 1e12},
         "gpu_launches": int(launches),
-        "e2e": {"value": world * T / (e2e_step / 1e3), "unit": UNIT,
+        "e2e": {"value": job_throughput(world, T, e2e_step), "unit": UNIT,
                 "h2d_bytes_per_step": T * fam.hidden * 2, "d2h_bytes_per_step": T * fam.hidden * 2,
                 "ms_per_step": e2e_step},
         "wall_s_timed_region": t_wall,
