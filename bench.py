@@ -52,6 +52,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm", "tcgemv"],
+                    help="force one of the layer's expert paths (default: the library's choice)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -236,6 +238,7 @@ def run_native(args, rank, local_rank, world):
     x = torch.from_numpy(xb.astype(np.int16)).view(torch.bfloat16).to(dev)
     out = torch.empty_like(x)
     layer = MoELayer(T, fam.hidden, fam.n_experts, fam.inter, k, local_rank)
+    layer.set_path(args.path)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     decode = T <= 64

@@ -97,6 +97,17 @@ cudaError_t launch_grouped_gemm(int mode, const TmapSet &tm, const int32_t *offs
                                 const float *w_scale, int E, int64_t H, int64_t I, int64_t Pmax,
                                 uint8_t *const h_terms[3], float *h_scale, float *y, int *err,
                                 int64_t max_items, int sms, cudaStream_t s);
+// Tokens per tile of the tensor-core grouped GEMV (its MMA N).
+constexpr int kDecodeTileN = 16;
+// Tensor-core grouped GEMV for small batches (tiles of kDecodeTileN tokens,
+// tile_offsets counted in such tiles).  mode 1: gate/up + SwiGLU -> h as
+// three e4m3 terms with one power-of-two scale per (position, 64 outputs),
+// h_scale [I/64][Pmax]; mode 2: down -> f32 y.
+cudaError_t launch_decode_mma(int mode, const TmapSet &tm, const int32_t *offsets,
+                              const int32_t *tile_offsets, const float *act_scale,
+                              const float *w_scale, int E, int64_t H, int64_t I, int64_t Pmax,
+                              uint8_t *const h_terms[3], float *h_scale, float *y, int *err,
+                              int64_t max_items, int sms, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const int32_t *inv, const float *wts, int64_t T, int k,
                            int64_t H, __nv_bfloat16 *out, cudaStream_t s);
 

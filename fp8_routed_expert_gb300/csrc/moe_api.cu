@@ -39,8 +39,10 @@ struct moe_ctx {
   __half *x16 = nullptr;
   __nv_bfloat16 *xin = nullptr, *xout = nullptr;  // staging for the host-buffer entry point
   uint8_t *a_hi = nullptr, *a_lo = nullptr, *h_t[3] = {nullptr, nullptr, nullptr};
-  float *a_scale = nullptr, *h_scale = nullptr;  // [K/128][Pmax]
+  float *a_scale = nullptr;                      // [H/128][Pmax]
+  float *h_scale = nullptr;                      // [I/128][Pmax] (GEMM) or [I/64][Pmax] (TCGEMV)
   TmapSet tm_gemm1, tm_gemm2;                    // activation terms (workspace) + last weights
+  TmapSet tm_dec1, tm_dec2;                      // the same operands in boxes of 16 positions
   const void *tm_w13_ptr = nullptr, *tm_w2_ptr = nullptr;  // weights the maps in .b describe
   int *err = nullptr;
   int path = MOE_PATH_AUTO;
@@ -133,6 +135,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
   int path = c->path != MOE_PATH_AUTO ? c->path : (T <= kGemvMaxT ? MOE_PATH_GEMV : MOE_PATH_GEMM);
   if (path == MOE_PATH_GEMM && H % 256 != 0) path = MOE_PATH_GEMV;  // GEMM2 tiles are 256 wide
   const int64_t max_active = P < E ? P : E;
+  const int tile_m = path == MOE_PATH_TCGEMV ? kDecodeTileN : kTileM;
   const int ks = router_k_split(T, E, H, c->sms);
   const float gamma = router_gamma(T, H, ks);
   if (T <= kRouterWarpMaxT) {
@@ -140,7 +143,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
     CUDA_TRY(launch_route_decode(x, T, rw, rb, E, H, k, gamma, c->logits, c->wnorm, c->xnorm,
                                  path == MOE_PATH_GEMV ? c->x16 : nullptr, c->xscale, c->ticket,
                                  c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv, c->active,
-                                 c->n_active, c->tile_offsets, kTileM,
+                                 c->n_active, c->tile_offsets, tile_m,
                                  path == MOE_PATH_GEMV ? c->hmax : nullptr, c->err, s));
   } else {
     {
@@ -155,7 +158,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
     if (path == MOE_PATH_GEMV) CUDA_TRY(launch_x_to_f16(x, T, H, c->x16, c->xscale, s));
     {
       Timed tm(c, MOE_K_PERMUTE, s);
-      CUDA_TRY(launch_permute(c->idx, P, (int)E, kTileM, c->counts, c->offsets, c->perm, c->inv,
+      CUDA_TRY(launch_permute(c->idx, P, (int)E, tile_m, c->counts, c->offsets, c->perm, c->inv,
                               c->active, c->n_active, c->tile_offsets,
                               path == MOE_PATH_GEMV ? c->hmax : nullptr, nullptr, 0, c->err, s));
     }
@@ -181,22 +184,39 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
       if (!encode_u8_tmap(&c->tm_gemm2.b, w2, I, E * H, 64)) return MOE_ERR_CUDA;
       c->tm_w2_ptr = w2;
     }
-    const int64_t max_tiles = (P + kTileM - 1) / kTileM + max_active;
+    c->tm_dec1.b = c->tm_gemm1.b;
+    c->tm_dec2.b = c->tm_gemm2.b;
+    const int64_t max_tiles = (P + tile_m - 1) / tile_m + max_active;
     {
       Timed tm(c, MOE_K_ACT_QUANT, s);
       CUDA_TRY(launch_act_quant(x, c->perm, P, k, H, Pm, c->a_hi, c->a_lo, c->a_scale, c->sms, s));
     }
-    {
-      Timed tm(c, MOE_K_GATE_UP, s);
-      CUDA_TRY(launch_grouped_gemm(1, c->tm_gemm1, c->offsets, c->tile_offsets, c->a_scale, s13,
+    if (path == MOE_PATH_TCGEMV) {
+      {
+        Timed tm(c, MOE_K_GATE_UP, s);
+        CUDA_TRY(launch_decode_mma(1, c->tm_dec1, c->offsets, c->tile_offsets, c->a_scale, s13,
                                    (int)E, H, I, Pm, c->h_t, c->h_scale, nullptr, c->err,
-                                   max_tiles * (I / 128), c->sms, s));
-    }
-    {
-      Timed tm(c, MOE_K_DOWN, s);
-      CUDA_TRY(launch_grouped_gemm(2, c->tm_gemm2, c->offsets, c->tile_offsets, c->h_scale, s2,
+                                   max_tiles * (I / 64), c->sms, s));
+      }
+      {
+        Timed tm(c, MOE_K_DOWN, s);
+        CUDA_TRY(launch_decode_mma(2, c->tm_dec2, c->offsets, c->tile_offsets, c->h_scale, s2,
                                    (int)E, H, I, Pm, nullptr, nullptr, c->y, c->err,
-                                   max_tiles * (H / 256), c->sms, s));
+                                   max_tiles * (H / 128), c->sms, s));
+      }
+    } else {
+      {
+        Timed tm(c, MOE_K_GATE_UP, s);
+        CUDA_TRY(launch_grouped_gemm(1, c->tm_gemm1, c->offsets, c->tile_offsets, c->a_scale, s13,
+                                     (int)E, H, I, Pm, c->h_t, c->h_scale, nullptr, c->err,
+                                     max_tiles * (I / 128), c->sms, s));
+      }
+      {
+        Timed tm(c, MOE_K_DOWN, s);
+        CUDA_TRY(launch_grouped_gemm(2, c->tm_gemm2, c->offsets, c->tile_offsets, c->h_scale, s2,
+                                     (int)E, H, I, Pm, nullptr, nullptr, c->y, c->err,
+                                     max_tiles * (H / 256), c->sms, s));
+      }
     }
   }
   {
@@ -306,7 +326,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->h_t[0], (size_t)(Pr * I)},
       {(void **)&c->h_t[1], (size_t)(Pr * I)},
       {(void **)&c->h_t[2], (size_t)(Pr * I)},
-      {(void **)&c->h_scale, (size_t)(I / 128 * Pm) * 4},
+      {(void **)&c->h_scale, (size_t)(I / 64 * Pm) * 4},
   };
   size_t total = 0;
   for (auto &s : slots) total += align_up(s.bytes, 256);
@@ -331,7 +351,13 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       !encode_u8_tmap(&c->tm_gemm1.a[2], c->a_lo, H, Pr, 128) ||
       !encode_u8_tmap(&c->tm_gemm2.a[0], c->h_t[0], I, Pr, 128) ||
       !encode_u8_tmap(&c->tm_gemm2.a[1], c->h_t[1], I, Pr, 128) ||
-      !encode_u8_tmap(&c->tm_gemm2.a[2], c->h_t[2], I, Pr, 128)) {
+      !encode_u8_tmap(&c->tm_gemm2.a[2], c->h_t[2], I, Pr, 128) ||
+      !encode_u8_tmap(&c->tm_dec1.a[0], c->a_hi, H, Pr, kDecodeTileN) ||
+      !encode_u8_tmap(&c->tm_dec1.a[1], c->a_lo, H, Pr, kDecodeTileN) ||
+      !encode_u8_tmap(&c->tm_dec1.a[2], c->a_lo, H, Pr, kDecodeTileN) ||
+      !encode_u8_tmap(&c->tm_dec2.a[0], c->h_t[0], I, Pr, kDecodeTileN) ||
+      !encode_u8_tmap(&c->tm_dec2.a[1], c->h_t[1], I, Pr, kDecodeTileN) ||
+      !encode_u8_tmap(&c->tm_dec2.a[2], c->h_t[2], I, Pr, kDecodeTileN)) {
     cudaFree(c->ws);
     delete c;
     return MOE_ERR_CUDA;
@@ -415,7 +441,9 @@ int moe_status(moe_ctx *c) {
 
 int moe_set_path(moe_ctx *c, int path) {
   if (c == nullptr) return MOE_ERR_ARG;
-  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GEMM) return MOE_ERR_ARG;
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_GEMV && path != MOE_PATH_GEMM &&
+      path != MOE_PATH_TCGEMV)
+    return MOE_ERR_ARG;
   c->path = path;
   return MOE_OK;
 }

@@ -11,7 +11,8 @@ import torch
 
 from ._lib import C, MoEConfig, check, lib
 
-PATHS = {"auto": C["MOE_PATH_AUTO"], "gemv": C["MOE_PATH_GEMV"], "gemm": C["MOE_PATH_GEMM"]}
+PATHS = {"auto": C["MOE_PATH_AUTO"], "gemv": C["MOE_PATH_GEMV"], "gemm": C["MOE_PATH_GEMM"],
+         "tcgemv": C["MOE_PATH_TCGEMV"]}
 KERNELS = {name: C[f"MOE_K_{name.upper()}"] for name in
            ("router_logits", "router_select", "permute", "gate_up", "down", "combine", "act_quant",
             "route")}

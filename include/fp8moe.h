@@ -145,11 +145,17 @@ const char *moe_strerror(int code);
 /*
  * Path selection.  MOE_PATH_AUTO picks the grouped-GEMV path for
  * T <= 64 and the tensor-core grouped-GEMM path above; the other values force
- * one path (both compute the same layer).
+ * one path (all compute the same layer).
+ *   MOE_PATH_GEMV   e4m3 weights dequantised in registers, mma.sync f16
+ *                   (activations as f16 hi/lo pairs);
+ *   MOE_PATH_GEMM   tcgen05 grouped GEMM, tiles of 128 positions;
+ *   MOE_PATH_TCGEMV tcgen05 grouped GEMV, tiles of 16 positions (the weight
+ *                   rows are the MMA's M operand, the expert's tokens its N).
  */
 #define MOE_PATH_AUTO 0
 #define MOE_PATH_GEMV 1
 #define MOE_PATH_GEMM 2
+#define MOE_PATH_TCGEMV 3
 int moe_set_path(moe_ctx *ctx, int path);
 
 /*

@@ -33,7 +33,7 @@ def weights(name):
 
 # ------------------------------------------------------------------ full parity
 
-@pytest.mark.parametrize("path", ["gemv", "gemm"])
+@pytest.mark.parametrize("path", ["gemv", "gemm", "tcgemv"])
 def test_tiny(path):
     fam, w, dw = weights("tiny")
     x = W.make_x(fam, 4)
@@ -45,7 +45,7 @@ def test_tiny(path):
 
 
 @pytest.mark.parametrize("T", [1, 8])
-@pytest.mark.parametrize("path", ["gemv", "gemm"])
+@pytest.mark.parametrize("path", ["gemv", "gemm", "tcgemv"])
 def test_olmoe_decode(T, path):
     fam, w, dw = weights("olmoe_decode")
     x = W.make_x(fam, T)
@@ -68,6 +68,32 @@ def test_olmoe_ragged_batches(T):
     check_output(out, ref)
 
 
+@pytest.mark.parametrize("T", [2, 17, 65, 300])
+def test_tcgemv_ragged_batches(T):
+    """Tensor-core GEMV over tiles of 16 positions: experts with one partial
+    tile, several tiles and a ragged last tile."""
+    fam, w, dw = weights("olmoe_decode")
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, fam.top_k, "tcgemv")
+    ref = reference(x, w, fam.top_k)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref)
+    assert T < 300 or ref["counts"].max() > 16  # several tiles per expert
+
+
+@pytest.mark.parametrize("T", [1, 16, 64])
+def test_wide_decode_tcgemv(T):
+    fam, w, dw = weights("wide_decode")
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, fam.top_k, "tcgemv")
+    tokens = None if T <= 16 else np.r_[0:4, T - 4:T]
+    ref = reference(x, w, fam.top_k, tokens=tokens)
+    check_routing(r, ref, fam.n_experts)
+    check_output(out, ref, tokens)
+
+
 def test_intermediates_match_oracle():
     """Per-kernel parity: h after gate/up + SwiGLU and y after the down GEMV."""
     fam, w, dw = weights("olmoe_decode")
@@ -86,9 +112,9 @@ def test_intermediates_match_oracle():
     assert np.linalg.norm(y - ref_y) / np.linalg.norm(ref_y) < 1e-4
 
 
-@pytest.mark.parametrize("T", [16, 300])
-def test_gemm_path_y_matches_oracle(T):
-    """Per-kernel parity of the tensor-core path: y after the down GEMM
+@pytest.mark.parametrize("T,path", [(16, "gemm"), (300, "gemm"), (8, "tcgemv"), (300, "tcgemv")])
+def test_tensor_core_paths_y_match_oracle(T, path):
+    """Per-kernel parity of the tensor-core paths: y after the down GEMM
     (position order) against the oracle's per-pair y.  Two e4m3 terms hold
     the bf16 x exactly and three keep about 12 bits of h, so y stays near
     1e-5 relative."""
@@ -96,7 +122,7 @@ def test_gemm_path_y_matches_oracle(T):
     k = fam.top_k
     x = W.make_x(fam, T)
     layer = make_layer(fam, T)
-    out, r = run(layer, x, dw, k, "gemm")
+    out, r = run(layer, x, dw, k, path)
     ref = reference(x, w, k)
     check_routing(r, ref, fam.n_experts)
     check_output(out, ref)
