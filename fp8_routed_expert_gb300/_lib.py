@@ -58,6 +58,7 @@ def lib():
         "moe_free": ([vp], None),
         "moe_strerror": ([ctypes.c_int], ctypes.c_char_p),
         "moe_set_path": ([vp, ctypes.c_int], ctypes.c_int),
+        "moe_resolve_path": ([vp, i64], ctypes.c_int),
         "moe_set_timing": ([vp, ctypes.c_int], ctypes.c_int),
         "moe_kernel_time": ([vp, ctypes.c_int, ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),

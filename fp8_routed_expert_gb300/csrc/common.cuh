@@ -90,11 +90,24 @@ __device__ __forceinline__ void mma_16816(float d[4], uint32_t a0, uint32_t a1, 
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
-// silu(z) * u with silu(z) = z / (1 + e^-z).
-__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + __expf(-g)) * u; }
+// silu(z) * u with silu(z) = z / (1 + e^-z).  The fast division (about two
+// ulps) stays far below the precision at which h is kept, and has no slow
+// path for large or non-finite operands.
+__device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
 // Exact power of two 2^e for |e| < 127.
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// v * 2^e as two multiplications by representable powers of two (|e| <= 252):
+// exact whenever the result is a normal float, without a per-value ldexpf.
+struct Pow2 {
+  float f1, f2;
+  __device__ __forceinline__ float operator()(float v) const { return v * f1 * f2; }
+};
+__device__ __forceinline__ Pow2 pow2_factors(int e) {
+  const int a = e / 2;
+  return Pow2{exp2i(a), exp2i(e - a)};
+}
 
 // Power-of-two exponent that brings a non-negative magnitude m to at most
 // 2^14 (the f16 conversion range used by the tensor-core GEMV); 0 if it

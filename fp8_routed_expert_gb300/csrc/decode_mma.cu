@@ -1,30 +1,47 @@
-// Grouped GEMV of the routed experts for small batches on the 5th-generation
-// tensor cores: each expert's weight rows are the MMA's M = 128 operand and
-// its (at most 16 per tile) tokens the N = 16 operand, so the weights stream
-// from HBM through TMA into shared memory and into tcgen05.mma without any
-// per-byte instruction on the SM.  The bytes moved per token decide MoE speed
-// (DeepSeek-V4.1-Flash post, "Bytes per token decide everything"); here the SM
-// only promotes one 128 x 16 partial per K block.
+// Routed-expert FFN for small batches on the 5th-generation tensor cores, in
+// ONE persistent launch: gate/up + SwiGLU for every (expert tile, 128 h
+// outputs), then down for every (expert tile, 256 output rows).
 //
-// Operands: A = e4m3 weight rows (one f32 scale per 128 x 128 block); B = the
-// expert's activation rows in position order, split into e4m3 terms sharing a
-// power-of-two scale per (row, K block): two terms for x (exact for bf16),
-// three for h.  The terms sit side by side along N (N = 32 or 48), so one MMA
-// per 32-wide K slice reads each weight byte from shared memory once; the
-// promotion adds the terms' columns.  Every 128-wide K block (64-wide for h,
-// whose scale is per 64 columns) is accumulated in its own TMEM buffer and
-// added to f32 registers as partial * s_w[row block, kb] * s_act[token, block]
-// (dragon.c §8 "Round 3": the block scale is folded out of the inner product).
+// The time of a decode step goes to moving expert weight bytes (DeepSeek-
+// V4.1-Flash post, "Bytes per token decide everything"), so the kernel is
+// built to stream them: each item's 256 weight rows are the MMA's N = 256
+// operand, loaded by TMA in 32 KiB stages (one or two boxes) and multiplied
+// in shared memory by tcgen05.mma without any per-byte instruction on the SM;
+// one M64 x N256 x K32 MMA covers 8 KiB of weights.
 //
-//   MODE 1 (gate/up): item = (16-token tile of expert e, h outputs i0..i0+63);
-//     A rows 0..63 are gate rows i0.., rows 64..127 the up rows I + i0..; the
-//     epilogue forms h = silu(gate) * up and writes it as three e4m3 terms with
-//     one power-of-two scale per (position, 64 outputs).
-//   MODE 2 (down): item = (16-token tile, output rows j0..j0+127); y in f32.
-// Warp 0 issues the TMA loads of each stage and, with 4-byte cp.async into a
-// ring of its own, the stage's scales (so they arrive with the weights instead
-// of behind them); warp 1 allocates TMEM and issues the MMAs; warps 2..5
-// promote and finish the item.  Every mbarrier wait is bounded.
+// Operands.  B = e4m3 weight rows (one f32 scale per 128 x 128 block).
+// A = the tile's activations as e4m3 terms that share one power-of-two scale
+// per (row, 128-column block); each term is its own MMA into the same TMEM
+// accumulator, so the terms add up in the tensor core.  Gate/up reads x (two
+// terms hold a bf16 value exactly), token-major, gathered four rows at a time
+// by TMA (tile::gather4) from the tile's token list into the first four rows of
+// each 8-row 128-byte-swizzle atom: position j of the tile is A row
+// 8 (j / 4) + j % 4 (a tile holds 32 positions; the other rows are never read
+// back).  Down reads h (three terms, about 12 bits) in position order, 32
+// rows per term.  Every 128-wide K block is accumulated in one of two TMEM
+// buffers and promoted in f32 registers as partial * s_w[row block, kb] *
+// s_act[row, kb] (dragon.c §8 "Round 3": the block scale is folded out of the
+// inner product), while the MMA fills the other buffer.
+//
+// Phases.  CTA c owns a contiguous share of the gate/up items and one of the
+// down items (counted from the other end of the list, so that the CTAs with
+// more gate/up work get less down work) and runs them in that order.  A down
+// item needs h of its tile, i.e. every gate/up item of the tile (possibly
+// other CTAs'): each CTA publishes its gate/up items on per-tile counters when
+// it has finished them, and the activation producer of a down item waits
+// (bounded) until the tile's counter is complete.  The weights do not depend
+// on h, so the weight producer runs ahead across the phase boundary and HBM
+// stays busy.  All CTAs are resident (one per SM, grid <= SMs) and every
+// gate/up item precedes every down item in each CTA's order, so the waits end.
+//
+// Accumulator layout (M = 64, one CTA): row 16 q + l sits in TMEM lane
+// 32 q + l for l < 16.  The epilogue reads it with tcgen05.ld.16x64b: in the
+// warp of lane quarter q, thread t holds row 16 q + (t >> 2) + 8 (t & 1) and,
+// of every 64 columns, those with parity (t >> 1) & 1, so the two threads of
+// a row (t and t ^ 2) split its columns and every thread carries data.
+// Warps: 0 weight TMA; 1 TMEM allocation and MMA issue; 2 activation TMA;
+// 4..7 promotion and epilogue (warp w reads lane quarter w % 4); 3 idle.
+// Every mbarrier wait and the counter wait are bounded by wall-clock time.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100_ptx.cuh"
@@ -34,136 +51,156 @@ using namespace sm100;
 
 namespace {
 
-constexpr int DM = 128;      // weight rows per item
-constexpr int DN = 16;       // tokens per tile
-constexpr int DK = 128;      // K per stage
-constexpr int A_BYTES = DM * DK;
-constexpr int B_BYTES = DN * DK;
-constexpr int MAX_NBUF = 8;  // TMEM partial buffers (see DPipe)
-constexpr int EPI_WARPS = 4;
-constexpr int SC_SLOTS = 24;   // scale ring slots, one per stage
-constexpr int SC_STRIDE = 36;  // floats per slot: 2 x 16 activation scales, 2 weight scales, pad
+constexpr int BM = 64;                 // MMA M: A rows (positions, per term)
+constexpr int TP = kDecodeTileN;       // positions per tile (32)
+constexpr int BN = 256;                // weight rows per item
+constexpr int BK = 128;                // K per stage
+constexpr int AX_TERM = 8 * 1024;      // x term: 8 atoms of 8 rows, 4 filled
+constexpr int AH_TERM = TP * BK;       // h term: 32 rows (4 KiB)
+constexpr int A_REGION = 2 * AX_TERM;  // 16 KiB (also holds 3 h terms + the 4 KiB read past the last)
+constexpr int B_BYTES = BN * BK;       // 32 KiB
+constexpr int STAGE = A_REGION + B_BYTES;
+constexpr int STAGES = 4;
+constexpr uint32_t TMEM_COLS = 512;    // two 256-column accumulators
+constexpr int EPI_THREADS = 128;       // warps 4..7
 constexpr int kMaxE = 1024;
-constexpr int DTHREADS = 64 + 32 * EPI_WARPS;
+constexpr int DTHREADS = 32 * 8;
+constexpr size_t DSMEM = (size_t)STAGES * STAGE + 1024;
 constexpr uint64_t DWAIT_NS = 2000000000ull;
 
-template <int NT>
-struct DPipe {
-  static constexpr int STAGE = A_BYTES + NT * B_BYTES;  // 20 KiB (NT=2) / 22 KiB (NT=3)
-  static constexpr int STAGES = 8;
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE + 1024;
-  static constexpr int NC = NT * DN;                     // MMA N: the terms side by side
-  static constexpr int BUF_COLS = NC <= 32 ? 32 : 64;    // TMEM columns per partial buffer
-  // gate/up: 8 buffers, so the MMAs run on while an item's SwiGLU and
-  // quantisation tail is computed; down (a short tail): 4
-  static constexpr int NBUF = NT == 2 ? 8 : 4;
-  static constexpr uint32_t TMEM_COLS = NBUF * BUF_COLS; // 256
-};
+static_assert(TP == 32, "tile of 32 positions: 8 gather atoms of 4 rows");
+static_assert(3 * AH_TERM + (BM - TP) * BK <= A_REGION + B_BYTES, "h MMA reads stay in the stage");
 
-struct DecodeArgs {
-  const int32_t *offsets, *tile_offsets;  // tile offsets in units of DN-token tiles
-  const float *act_scale;                 // [K/blk][Pmax], blk = 128 (x) or 64 (h)
-  const float *w_scale;                   // s13 or s2
+struct FfnArgs {
+  const int32_t *offsets, *tile_offsets;  // tile offsets in units of TP-position tiles
+  const int32_t *perm;                    // position -> pair id t * k + r
+  int k;
+  const float *x_scale;                   // [H/128][x_ld] per token
+  int64_t x_ld;
+  const float *s13, *s2;
   int E;
   int64_t H, I, Pmax;
-  int n_blocks;                           // MODE 1: I/64, MODE 2: H/128
-  uint8_t *h_t0, *h_t1, *h_t2;            // MODE 1 outputs [Pmax, I]
-  float *h_scale;                         // [I/64][Pmax]
-  float *y;                               // MODE 2 output [Pmax, H]
+  uint8_t *h_t0, *h_t1, *h_t2;            // [Pmax, I] three terms of h
+  float *h_scale;                         // [I/128][Pmax]
+  float *y;                               // [Pmax, H]
+  int32_t *done13;                        // finished gate/up items per tile (0 at entry)
   int *err;
 };
 
 struct DItem {
   int e, nb;
+  int64_t tile;       // global tile index
   int64_t p0, p_end;  // first position of the tile, end of the expert's segment
+  int nvalid;         // positions of this tile (1..TP)
 };
 
-// Item -> (expert, row block, tile positions), from shared-memory copies of
-// the tile and position offsets.
-__device__ __forceinline__ DItem ditem(const int *toff, const int *off, int E, int n_blocks,
-                                       int64_t item) {
+__device__ __forceinline__ DItem ditem(const int *toff, const int *off, int E, int n_blocks, int64_t item) {
   DItem c;
-  const int64_t ti = item / n_blocks;
+  c.tile = item / n_blocks;
   c.nb = (int)(item % n_blocks);
   int lo = 0, hi = E;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (toff[mid] <= ti) lo = mid;
+    if (toff[mid] <= c.tile) lo = mid;
     else hi = mid;
   }
   c.e = lo;
-  c.p0 = off[lo] + (ti - toff[lo]) * DN;
+  c.p0 = off[lo] + (c.tile - toff[lo]) * TP;
   c.p_end = off[lo + 1];
+  const int64_t n = c.p_end - c.p0;
+  c.nvalid = (int)(n < TP ? n : TP);
   return c;
 }
 
-// 32 lanes x 16 consecutive f32 columns of TMEM (no wait).
-__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t *v) {
+// The CTA's work list: gate/up items [lo1, lo1 + n1), then down items
+// [lo2, lo2 + n2).
+struct Plan {
+  int64_t lo1, n1, lo2, n2;
+  int nb1, nb2;  // column blocks per tile: I/128 (gate/up), H/256 (down)
+  __device__ __forceinline__ int64_t count() const { return n1 + n2; }
+  __device__ __forceinline__ bool down(int64_t q) const { return q >= n1; }
+  __device__ __forceinline__ int64_t item(int64_t q) const { return q < n1 ? lo1 + q : lo2 + (q - n1); }
+  __device__ __forceinline__ int nblocks(int64_t q) const { return q < n1 ? nb1 : nb2; }
+};
+
+// Four rows of a 2-D tensor (box of one row) into consecutive 128-byte rows
+// of shared memory; the destination is the start of a 1024-byte swizzle atom.
+__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *m, int32_t x, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3, uint64_t *bar) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
-        "=r"(v[14]), "=r"(v[15])
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void fail(volatile int *abort_flag, int *err) {
+  *abort_flag = 1;
+  set_error(err, DEV_ERR_TIMEOUT);
+}
+
+// 16 lanes x 64 columns (tcgen05.ld.16x64b.x32, no wait): value i of thread
+// t is lane (t >> 2) + 8 (t & 1), column 2 i + ((t >> 1) & 1).
+__device__ __forceinline__ void tmem_ld16x64(uint32_t taddr, float *v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x64b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 4-byte asynchronous copy global -> shared, tracked by cp.async.mbarrier.arrive.
-__device__ __forceinline__ void cp_async4(float *dst, const float *src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-
-// Arrive on `bar` once this thread's earlier cp.async copies have landed
-// (without first raising the pending count: the barrier's count includes
-// this thread).
-__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-template <int MODE, int NT>
-__global__ void __launch_bounds__(DTHREADS, 1) decode_mma_kernel(const __grid_constant__ TmapSet tm,
-                                                                 const DecodeArgs p) {
-  constexpr int STAGES = DPipe<NT>::STAGES, STAGE = DPipe<NT>::STAGE;
-  constexpr int NBUF = DPipe<NT>::NBUF;
-  constexpr int KSUB = (MODE == 1) ? 1 : 2;  // promotions per 128-wide K stage
+__global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_constant__ DecodeMaps tm,
+                                                                 const FfnArgs p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[STAGES], empty_bar[STAGES], tfull[MAX_NBUF],
-      tempty[MAX_NBUF], sc_full[SC_SLOTS], sc_empty[SC_SLOTS];
-  __shared__ __align__(16) float sc_ring[SC_SLOTS][SC_STRIDE];
+  __shared__ __align__(8) uint64_t full_a[STAGES], full_b[STAGES], empty_bar[STAGES], tfull[2], tempty[2];
   __shared__ int s_toff[kMaxE + 1], s_off[kMaxE + 1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
-  __shared__ float upbuf[64][DN + 1];
-  __shared__ float colmax[2][DN];
+  __shared__ int32_t s_rows[TP];  // token rows of the activation producer's current tile
 
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t K = MODE == 1 ? p.H : p.I;
-  const int64_t nkb = K / DK;
+  const int64_t nkb1 = p.H / BK, nkb2 = p.I / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_a[s], 1);
+      mbar_init(&full_b[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
-    for (int b = 0; b < NBUF; ++b) {
+    for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], EPI_WARPS);
-    }
-    for (int s = 0; s < SC_SLOTS; ++s) {
-      mbar_init(&sc_full[s], 32);  // every lane of the producer warp arrives
-      mbar_init(&sc_empty[s], EPI_WARPS);
+      mbar_init(&tempty[b], EPI_THREADS / 32);
     }
     abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, DPipe<NT>::TMEM_COLS);
+    tmem_alloc(&tmem_base_sh, TMEM_COLS);
     tmem_relinquish();
     tc_fence_before();
   }
-  pdl_wait();  // routing and activation terms come from earlier kernels of the stream
+  pdl_wait();  // routing and activation terms come from the previous kernel
   pdl_trigger();
   for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
     s_toff[i] = p.tile_offsets[i];
@@ -172,212 +209,341 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_mma_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const int64_t n_items = (int64_t)s_toff[p.E] * p.n_blocks;
-  const int64_t it_lo = n_items * blockIdx.x / gridDim.x, it_hi = n_items * (blockIdx.x + 1) / gridDim.x;
-  const int64_t wblocks = MODE == 1 ? 2 * p.I / 128 : p.H / 128;
+
+  Plan plan;
+  plan.nb1 = (int)(p.I / 128);
+  plan.nb2 = (int)(p.H / 256);
+  {
+    const int64_t n_tiles = s_toff[p.E];
+    const int64_t n1 = n_tiles * plan.nb1, n2 = n_tiles * plan.nb2;
+    const int64_t g = gridDim.x, b = blockIdx.x, rb = g - 1 - b;
+    plan.lo1 = n1 * b / g;
+    plan.n1 = n1 * (b + 1) / g - plan.lo1;
+    plan.lo2 = n2 * rb / g;
+    plan.n2 = n2 * (rb + 1) / g - plan.lo2;
+  }
+  const int64_t nq = plan.count();
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA + scales
-    // The whole warp walks the stages: lane 0 issues the TMA loads, every
-    // lane copies (at most) one activation scale and lanes 16/17 or 0 the
-    // weight scales; each lane then arrives on the slot's barrier.
+    // ---------------------------------------------------------------- weight TMA
+    // The whole warp walks the stages (waits are warp-uniform); lane 0 issues.
     if (lane == 0) {
-      for (int t = 0; t < NT; ++t) prefetch_tmap(&tm.a[t]);
-      prefetch_tmap(&tm.b);
+      prefetch_tmap(&tm.w13);
+      prefetch_tmap(&tm.w2);
     }
-    const int a_sub = lane >> 4, a_j = lane & 15;
-    int stage = 0, sslot = 0;
-    uint32_t phase = 0, sphase = 0;
+    int stage = 0;
+    uint32_t phase = 0;
     bool run = true;
-    for (int64_t item = it_lo; item < it_hi && run; ++item) {
-      const DItem c = ditem(s_toff, s_off, p.E, p.n_blocks, item);
-      int64_t r0, r1, wb;
-      if (MODE == 1) {
-        r0 = (int64_t)c.e * 2 * p.I + (int64_t)c.nb * 64;
-        r1 = r0 + p.I;
-        // lane 16: gate rows' scale block, lane 17: up rows'
-        wb = (lane == 16 ? 0 : p.I) / 128 + (int64_t)c.nb * 64 / 128;
-      } else {
-        r0 = (int64_t)c.e * p.H + (int64_t)c.nb * 128;
-        r1 = r0 + 64;
-        wb = c.nb;
-      }
-      const float *ws = p.w_scale + (int64_t)c.e * wblocks * nkb;
-      const int64_t apos = c.p0 + a_j;
+    for (int64_t q = 0; q < nq && run; ++q) {
+      const bool dn = plan.down(q);
+      const DItem c = ditem(s_toff, s_off, p.E, plan.nblocks(q), plan.item(q));
+      const int64_t r0 = dn ? (int64_t)c.e * p.H + (int64_t)c.nb * 256       // 256 W2 rows
+                            : (int64_t)c.e * 2 * p.I + (int64_t)c.nb * 128;  // 128 gate rows
+      const int64_t nkb = dn ? nkb2 : nkb1;
       for (int64_t kb = 0; kb < nkb; ++kb) {
-        if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag, DWAIT_NS)) {
-          abort_flag = 1;
-          set_error(p.err, DEV_ERR_TIMEOUT);
+        // every lane waits; the outcome is made warp-uniform
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag, DWAIT_NS))) {
+          if (lane == 0) fail(&abort_flag, p.err);
           run = false;
           break;
         }
         if (lane == 0) {
-          uint8_t *st = smem + (size_t)stage * STAGE;
-          mbar_arrive_expect_tx(&full_bar[stage], STAGE);
-          const int32_t kx = (int32_t)(kb * DK);
-          tma_load_2d(st, &tm.b, kx, (int32_t)r0, &full_bar[stage]);
-          tma_load_2d(st + A_BYTES / 2, &tm.b, kx, (int32_t)r1, &full_bar[stage]);
-#pragma unroll
-          for (int t = 0; t < NT; ++t)
-            tma_load_2d(st + A_BYTES + t * B_BYTES, &tm.a[t], kx, (int32_t)c.p0, &full_bar[stage]);
+          uint8_t *sb = smem + (size_t)stage * STAGE + A_REGION;
+          mbar_arrive_expect_tx(&full_b[stage], B_BYTES);
+          const int32_t kx = (int32_t)(kb * BK);
+          if (dn) {
+            tma_load_2d(sb, &tm.w2, kx, (int32_t)r0, &full_b[stage]);
+          } else {
+            tma_load_2d(sb, &tm.w13, kx, (int32_t)r0, &full_b[stage]);                      // gate
+            tma_load_2d(sb + B_BYTES / 2, &tm.w13, kx, (int32_t)(r0 + p.I), &full_b[stage]);  // up
+          }
         }
+        __syncwarp();
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-
-        if (!mbar_wait(&sc_empty[sslot], sphase ^ 1u, &abort_flag, DWAIT_NS)) {
-          abort_flag = 1;
-          set_error(p.err, DEV_ERR_TIMEOUT);
+      }
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- activation TMA
+    if (lane == 0) {
+      prefetch_tmap(&tm.x[0]);
+      prefetch_tmap(&tm.x[1]);
+      for (int t = 0; t < 3; ++t) prefetch_tmap(&tm.h[t]);
+    }
+    int stage = 0;
+    uint32_t phase = 0;
+    bool run = true;
+    for (int64_t q = 0; q < nq && run; ++q) {
+      const bool dn = plan.down(q);
+      const DItem c = ditem(s_toff, s_off, p.E, plan.nblocks(q), plan.item(q));
+      const int64_t nkb = dn ? nkb2 : nkb1;
+      int32_t tok = 0;
+      if (!dn) {
+        // token of each of the tile's positions (lane j); padding positions
+        // repeat the tile's first token and their rows are never read back
+        tok = __ldg(p.perm + c.p0 + (lane < c.nvalid ? lane : 0)) / p.k;
+      } else {
+        // down: wait until every gate/up item of this tile has published h
+        bool ok = true;
+        if (lane == 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire(p.done13 + c.tile) < plan.nb1) {
+            if (abort_flag || global_timer_ns() - t0 > DWAIT_NS) { ok = false; break; }
+          }
+          fence_proxy_async_global();
+        }
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) {
+          if (lane == 0) fail(&abort_flag, p.err);
+          break;
+        }
+      }
+      const int n_atoms = (c.nvalid + 3) / 4;
+      __syncwarp();
+      s_rows[lane] = tok;
+      __syncwarp();
+      for (int64_t kb = 0; kb < nkb; ++kb) {
+        // every lane waits; the outcome is made warp-uniform
+        if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag, DWAIT_NS))) {
+          if (lane == 0) fail(&abort_flag, p.err);
           run = false;
           break;
         }
-        float *sc = sc_ring[sslot];
-        if (a_sub < KSUB && apos < p.Pmax)
-          cp_async4(sc + a_sub * DN + a_j, p.act_scale + (kb * KSUB + a_sub) * p.Pmax + apos);
-        if (MODE == 1 ? (lane == 16 || lane == 17) : lane == 0)
-          cp_async4(sc + 2 * DN + (MODE == 1 ? lane - 16 : 0), ws + wb * nkb + kb);
-        cp_async_arrive(&sc_full[sslot]);
-        if (++sslot == SC_SLOTS) { sslot = 0; sphase ^= 1u; }
+        if (lane == 0) {
+          uint8_t *sa = smem + (size_t)stage * STAGE;
+          const int32_t kx = (int32_t)(kb * BK);
+          if (!dn) {
+            mbar_arrive_expect_tx(&full_a[stage], (uint32_t)(2 * n_atoms * 512));
+            for (int t = 0; t < 2; ++t)
+              for (int g = 0; g < n_atoms; ++g)  // atom g of term t: 1024-byte aligned
+                tma_gather4(sa + t * AX_TERM + g * 1024, &tm.x[t], kx, s_rows[4 * g], s_rows[4 * g + 1],
+                            s_rows[4 * g + 2], s_rows[4 * g + 3], &full_a[stage]);
+          } else {
+            mbar_arrive_expect_tx(&full_a[stage], 3 * AH_TERM);
+#pragma unroll
+            for (int t = 0; t < 3; ++t)
+              tma_load_2d(sa + t * AH_TERM, &tm.h[t], kx, (int32_t)c.p0, &full_a[stage]);
+          }
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      constexpr int NC = DPipe<NT>::NC;
-      const uint32_t idesc = idesc_e4m3_f32(DM, NC);
-      int stage = 0, buf = 0;
-      uint32_t phase = 0, bphase = 0;
-      for (int64_t item = it_lo; item < it_hi && !abort_flag; ++item) {
-        for (int64_t kb = 0; kb < nkb && !abort_flag; ++kb) {
-          if (!mbar_wait(&full_bar[stage], phase, &abort_flag, DWAIT_NS)) {
-            abort_flag = 1;
-            set_error(p.err, DEV_ERR_TIMEOUT);
-            break;
-          }
+    // The whole warp walks the stages (waits are warp-uniform); lane 0 issues.
+    const uint32_t idesc = idesc_e4m3_f32(BM, BN);
+    int stage = 0, buf = 0;
+    uint32_t phase = 0, bphase = 0;
+    bool run = true;
+    for (int64_t q = 0; q < nq && run; ++q) {
+      const bool dn = plan.down(q);
+      const int64_t nkb = dn ? nkb2 : nkb1;
+      for (int64_t kb = 0; kb < nkb; ++kb) {
+        const bool ready = mbar_wait(&full_b[stage], phase, &abort_flag, DWAIT_NS) &&
+                           mbar_wait(&full_a[stage], phase, &abort_flag, DWAIT_NS) &&
+                           mbar_wait(&tempty[buf], bphase ^ 1u, &abort_flag, DWAIT_NS);
+        if (!__all_sync(0xffffffffu, ready)) {
+          if (lane == 0) fail(&abort_flag, p.err);
+          run = false;
+          break;
+        }
+        tc_fence_after();
+        if (lane == 0) {
           const uint32_t a = smem_u32(smem + (size_t)stage * STAGE);
-          const uint32_t b = a + A_BYTES;
+          const uint64_t bdesc = sw128_kmajor_desc(a + A_REGION);
+          const uint64_t adesc = sw128_kmajor_desc(a);
+          const uint32_t d = tmem + (uint32_t)(buf * BN);
+          if (dn) {
 #pragma unroll
-          for (int sub = 0; sub < KSUB; ++sub) {
-            if (!mbar_wait(&tempty[buf], bphase ^ 1u, &abort_flag, DWAIT_NS)) {
-              abort_flag = 1;
-              set_error(p.err, DEV_ERR_TIMEOUT);
-              break;
-            }
-            tc_fence_after();
-            const uint32_t d = tmem + (uint32_t)(buf * DPipe<NT>::BUF_COLS);
+            for (int kk = 0; kk < BK / 32; ++kk)
 #pragma unroll
-            for (int kk = sub * (4 / KSUB); kk < (sub + 1) * (4 / KSUB); ++kk)
-              mma_f8f6f4(d, sw128_kmajor_desc(a + kk * 32), sw128_kmajor_desc(b + kk * 32), idesc,
-                         kk > sub * (4 / KSUB) ? 1u : 0u);
-            mma_commit(&tfull[buf]);
-            if (++buf == NBUF) { buf = 0; bphase ^= 1u; }
+              for (int t = 0; t < 3; ++t)  // the descriptor's address field counts 16 bytes
+                mma_f8f6f4(d, adesc + (uint64_t)((t * AH_TERM + kk * 32) >> 4), bdesc + (uint64_t)(kk * 2),
+                           idesc, (kk > 0 || t > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < BK / 32; ++kk)
+#pragma unroll
+              for (int t = 0; t < 2; ++t)
+                mma_f8f6f4(d, adesc + (uint64_t)((t * AX_TERM + kk * 32) >> 4), bdesc + (uint64_t)(kk * 2),
+                           idesc, (kk > 0 || t > 0) ? 1u : 0u);
           }
           mma_commit(&empty_bar[stage]);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          mma_commit(&tfull[buf]);
         }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        buf ^= 1;
+        if (buf == 0) bphase ^= 1u;
       }
     }
-  } else {
+  } else if (warp >= 4) {
     // ---------------------------------------------------------------- promotion + epilogue
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // weight row of this thread within the item
-    const int w_idx = 2 * DN + ((MODE == 1 && r >= 64) ? 1 : 0);
+    const int quarter = warp & 3;                             // TMEM lanes 32 quarter .. + 15
+    const int row = quarter * 16 + (lane >> 2) + 8 * (lane & 1);  // accumulator (A) row
+    const int par = (lane >> 1) & 1;                          // parity of this thread's columns
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
-    int buf = 0, sslot = 0;
-    uint32_t bphase = 0, sphase = 0;
+    int buf = 0;
+    uint32_t bphase = 0;
     bool ok = true;
-    for (int64_t item = it_lo; item < it_hi; ++item) {
-      const DItem c = ditem(s_toff, s_off, p.E, p.n_blocks, item);
-      float acc[DN];
+    for (int64_t q = 0; q < nq; ++q) {
+      const bool dn = plan.down(q);
+      const DItem c = ditem(s_toff, s_off, p.E, plan.nblocks(q), plan.item(q));
+      const int64_t nkb = dn ? nkb2 : nkb1;
+      // position of this thread's row: x rows fill 4 of every 8 (gather atoms)
+      const int j = dn ? row : (row >> 3) * 4 + (row & 7);
+      const bool valid = dn ? (row < c.nvalid) : ((row & 7) < 4 && j < c.nvalid);
+      const int64_t pos = c.p0 + (valid ? j : 0);
+      const float *sa_p;
+      int64_t sa_ld;
+      if (!dn) {
+        sa_p = p.x_scale + __ldg(p.perm + pos) / p.k;
+        sa_ld = p.x_ld;
+      } else {
+        // h and its scales are written in this launch by other CTAs: acquire
+        // the tile's counter before reading them, and read them coherently
+        bool dep = true;
+        if (lane == 0) {
+          const uint64_t t0 = global_timer_ns();
+          while (ld_acquire(p.done13 + c.tile) < plan.nb1) {
+            if (abort_flag || global_timer_ns() - t0 > DWAIT_NS) { dep = false; break; }
+          }
+        }
+        if (__shfl_sync(0xffffffffu, dep ? 1 : 0, 0) == 0) fail(&abort_flag, p.err);
+        sa_p = p.h_scale + pos;
+        sa_ld = p.Pmax;
+      }
+      // x scales come from the previous kernel (read-only path); h scales
+      // from this one (L2, coherent)
+      auto ld_scale = [&](const float *a) -> float { return dn ? __ldcg(a) : __ldg(a); };
+      // weight scale rows of columns [0, 128) and [128, 256): gate / up rows
+      // (gate/up) or the item's two 128-row blocks (down)
+      const float *wsc = dn ? p.s2 + (int64_t)c.e * (p.H / 128) * nkb2
+                            : p.s13 + (int64_t)c.e * (2 * p.I / 128) * nkb1;
+      const int64_t wb0 = dn ? 2 * (int64_t)c.nb : c.nb;
+      const int64_t wb1 = dn ? 2 * (int64_t)c.nb + 1 : p.I / 128 + c.nb;
+      // acc[32 ch + i] = column 64 ch + 2 i + par
+      float acc[128];
 #pragma unroll
-      for (int j = 0; j < DN; ++j) acc[j] = 0.f;
-      for (int64_t kb = 0; kb < nkb && ok; ++kb) {
-        if (!mbar_wait(&sc_full[sslot], sphase, &abort_flag, DWAIT_NS)) {
-          abort_flag = 1;
-          set_error(p.err, DEV_ERR_TIMEOUT);
+      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
+      float sa_n = ld_scale(sa_p), s0_n = __ldg(wsc + wb0 * nkb), s1_n = __ldg(wsc + wb1 * nkb);
+      for (int64_t kb = 0; kb < nkb; ++kb) {
+        const float sa = sa_n, c0 = sa * s0_n, c1 = sa * s1_n;
+        if (kb + 1 < nkb) {  // next block's scales, in flight while this one is promoted
+          sa_n = ld_scale(sa_p + (kb + 1) * sa_ld);
+          s0_n = __ldg(wsc + wb0 * nkb + kb + 1);
+          s1_n = __ldg(wsc + wb1 * nkb + kb + 1);
+        }
+        if (!mbar_wait(&tfull[buf], bphase, &abort_flag, DWAIT_NS)) {
+          fail(&abort_flag, p.err);
           ok = false;
           break;
         }
-        const float *sc = sc_ring[sslot];
-        const float sw = sc[w_idx];
+        tc_fence_after();
+        const uint32_t tb = t_lane + (uint32_t)(buf * BN);
 #pragma unroll
-        for (int sub = 0; sub < KSUB; ++sub) {
-          if (!mbar_wait(&tfull[buf], bphase, &abort_flag, DWAIT_NS)) {
-            abort_flag = 1;
-            set_error(p.err, DEV_ERR_TIMEOUT);
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          uint32_t v[NT * DN];
-          const uint32_t ta = t_lane + (uint32_t)(buf * DPipe<NT>::BUF_COLS);
-          tmem_ld_x16(ta, v);
-          tmem_ld_x16(ta + DN, v + DN);
-          if (NT == 3) tmem_ld_x16(ta + 2 * DN, v + 2 * DN);
+        for (int ch = 0; ch < 4; ++ch) {
+          float v[32];
+          tmem_ld16x64(tb + (uint32_t)(64 * ch), v);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&tempty[buf]);
-          if (++buf == NBUF) { buf = 0; bphase ^= 1u; }
-          const float4 *sa4 = reinterpret_cast<const float4 *>(sc + sub * DN);
+          const float sc = ch < 2 ? c0 : c1;
 #pragma unroll
-          for (int j4 = 0; j4 < DN / 4; ++j4) {
-            const float4 sa = sa4[j4];
-            const float sj[4] = {sa.x, sa.y, sa.z, sa.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int j = j4 * 4 + u;
-              float t = __uint_as_float(v[j]) + __uint_as_float(v[DN + j]);
-              if (NT == 3) t += __uint_as_float(v[2 * DN + j]);
-              acc[j] = fmaf(t, sj[u] * sw, acc[j]);
-            }
-          }
+          for (int i = 0; i < 32; ++i) acc[ch * 32 + i] = fmaf(v[i], sc, acc[ch * 32 + i]);
         }
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sc_empty[sslot]);
-        if (++sslot == SC_SLOTS) { sslot = 0; sphase ^= 1u; }
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+        buf ^= 1;
+        if (buf == 0) bphase ^= 1u;
       }
-      // all four epilogue warps agree before the shared buffers are touched
-      ok = named_bar_and(1, 32 * EPI_WARPS, ok);
+      // all four epilogue warps agree before the next phase's shared state
+      ok = named_bar_and(1, EPI_THREADS, ok);
       if (!ok) break;
-      const int nvalid = (int)((c.p_end - c.p0) < DN ? (c.p_end - c.p0) : DN);
-      if (MODE == 1) {
-        // up rows hand their sums to the gate rows of the same h outputs
-        if (r >= 64)
+      if (!dn) {
+        // h = silu(gate) * up: gate column 64 ch + 2 i + par pairs with up
+        // column 128 + (the same); h output o = 64 ch + 2 i + par, ch in {0, 1}.
+        // The tail runs once per item, so its code is kept short (it is
+        // fetched cold once per CTA): loops over small unrolled bodies that
+        // rotate the accumulator registers instead of indexing them.
+        float amax = 0.f;
+#pragma unroll 1
+        for (int k = 0; k < 4; ++k) {  // 16 outputs per pass; afterwards acc[0..63] = h in order
+          float hv[16];
 #pragma unroll
-          for (int j = 0; j < DN; ++j) upbuf[r - 64][j] = acc[j];
-        named_bar_sync(1, 32 * EPI_WARPS);
-        float hv[DN];
-        if (r < 64) {
+          for (int i = 0; i < 16; ++i) {
+            hv[i] = valid ? swiglu(acc[i], acc[64 + i]) : 0.f;  // rows without a position hold garbage
+            amax = fmaxf(amax, fabsf(hv[i]));
+          }
 #pragma unroll
-          for (int j = 0; j < DN; ++j) {
-            if (j < nvalid) {  // the same for the whole CTA
-              hv[j] = swiglu(acc[j], upbuf[r][j]);
-              const float m = warp_max(fabsf(hv[j]));
-              if (lane == 0) colmax[r >> 5][j] = m;
+          for (int i = 0; i < 48; ++i) {
+            acc[i] = acc[i + 16];
+            acc[64 + i] = acc[80 + i];
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[48 + i] = hv[i];
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));  // the row's other parity
+        const int ex = e4m3_block_exponent(amax);
+        const Pow2 down = pow2_factors(-ex);
+        // three e4m3 terms per value; thread pairs assemble consecutive
+        // outputs: in each group of 8 outputs (4 per parity) the even thread
+        // stores groups 0, 2, .. and the odd thread groups 1, 3, ..
+        const int64_t off = pos * p.I + (int64_t)c.nb * 128;
+#pragma unroll 1
+        for (int g = 0; g < 16; ++g) {  // outputs [8 g, 8 g + 8) = acc[0..3] of each parity
+          uint32_t mine[3];
+          {
+            uint32_t a[3], b[3];
+            e4m3_terms<3>(down(acc[0]), down(acc[1]), a);
+            e4m3_terms<3>(down(acc[2]), down(acc[3]), b);
+#pragma unroll
+            for (int t = 0; t < 3; ++t) mine[t] = a[t] | (b[t] << 16);  // 4 codes, one byte each
+          }
+#pragma unroll
+          for (int i = 0; i < 60; ++i) acc[i] = acc[i + 4];
+          const int o = 64 * (g >> 3) + 8 * (g & 7);
+#pragma unroll
+          for (int t = 0; t < 3; ++t) {
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, mine[t], 2);
+            const uint32_t ev = par ? other : mine[t], od = par ? mine[t] : other;
+            // interleave: e0 o0 e1 o1 | e2 o2 e3 o3
+            const uint32_t lo = (ev & 0xffu) | ((od & 0xffu) << 8) | ((ev & 0xff00u) << 8) | ((od & 0xff00u) << 16);
+            const uint32_t hi = ((ev >> 16) & 0xffu) | (((od >> 16) & 0xffu) << 8) |
+                                ((ev >> 8) & 0xff0000u) | ((od & 0xff000000u));
+            uint8_t *dst = t == 0 ? p.h_t0 : (t == 1 ? p.h_t1 : p.h_t2);
+            if (valid && (g & 1) == par) *reinterpret_cast<uint2 *>(dst + off + o) = make_uint2(lo, hi);
+          }
+        }
+        if (valid && par == 0) p.h_scale[(int64_t)c.nb * p.Pmax + pos] = ldexpf(1.f, ex);
+        // after the CTA's last gate/up item, publish all of them: every
+        // epilogue thread makes its h stores visible to other CTAs' TMA reads
+        // (proxy fence, then gpu-scope fence), the barrier orders all of
+        // that before one counter increment per tile (for that tile's items)
+        if (q == plan.n1 - 1) {
+          fence_proxy_async_global();
+          __threadfence();
+          named_bar_sync(1, EPI_THREADS);
+          if (warp == 4 && lane == 0) {
+            __threadfence();
+            const int64_t t_lo = plan.lo1 / plan.nb1, t_hi = (plan.lo1 + plan.n1 - 1) / plan.nb1;
+            for (int64_t t = t_lo; t <= t_hi; ++t) {
+              const int64_t a = t * plan.nb1 > plan.lo1 ? t * plan.nb1 : plan.lo1;
+              const int64_t b = (t + 1) * plan.nb1 < plan.lo1 + plan.n1 ? (t + 1) * plan.nb1 : plan.lo1 + plan.n1;
+              atomicAdd(p.done13 + t, (int)(b - a));
             }
           }
         }
-        named_bar_sync(1, 32 * EPI_WARPS);
-        if (r < 64) {
-          const int64_t col = (int64_t)c.nb * 64 + r;
-#pragma unroll
-          for (int j = 0; j < DN; ++j) {
-            if (j >= nvalid) break;
-            const int ex = e4m3_block_exponent(fmaxf(colmax[0][j], colmax[1][j]));
-            uint32_t cd[3];
-            e4m3_terms<3>(ldexpf(hv[j], -ex), 0.f, cd);
-            const int64_t pos = c.p0 + j;
-            p.h_t0[pos * p.I + col] = (uint8_t)(cd[0] & 0xffu);
-            p.h_t1[pos * p.I + col] = (uint8_t)(cd[1] & 0xffu);
-            p.h_t2[pos * p.I + col] = (uint8_t)(cd[2] & 0xffu);
-            if (r == 0) p.h_scale[(int64_t)c.nb * p.Pmax + pos] = ldexpf(1.f, ex);
-          }
-        }
-        // upbuf / colmax are reused only after the next item's agreement barrier
       } else {
+        // y: value i of chunk ch is column 64 ch + 2 i + par (the row's other
+        // parity is stored by thread lane ^ 2); short code, rotating registers
+        float *dy = p.y + pos * p.H + (int64_t)c.nb * 256 + par;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
+          if (valid)
 #pragma unroll
-        for (int j = 0; j < DN; ++j) {
-          if (j >= nvalid) break;
-          p.y[(c.p0 + j) * p.H + (int64_t)c.nb * 128 + r] = acc[j];
+            for (int i = 0; i < 32; ++i) dy[64 * ch + 2 * i] = acc[i];
+#pragma unroll
+          for (int i = 0; i < 96; ++i) acc[i] = acc[i + 32];
         }
       }
     }
@@ -393,44 +559,45 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_mma_kernel(const __grid_co
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, DPipe<NT>::TMEM_COLS);
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_decode_mma(int mode, const TmapSet &tm, const int32_t *offsets,
-                              const int32_t *tile_offsets, const float *act_scale,
-                              const float *w_scale, int E, int64_t H, int64_t I, int64_t Pmax,
-                              uint8_t *const h_terms[3], float *h_scale, float *y, int *err,
-                              int64_t max_items, int sms, cudaStream_t s) {
-  DecodeArgs p;
+cudaError_t launch_decode_ffn(const DecodeMaps &maps, const int32_t *offsets,
+                              const int32_t *tile_offsets, const int32_t *perm, int k,
+                              const float *x_scale, int64_t x_ld, const float *s13, const float *s2,
+                              int E, int64_t H, int64_t I, int64_t Pmax, uint8_t *const h_terms[3],
+                              float *h_scale, float *y, int32_t *done13, int *err, int64_t max_tiles,
+                              int sms, cudaStream_t s) {
+  FfnArgs p;
   p.offsets = offsets;
   p.tile_offsets = tile_offsets;
-  p.act_scale = act_scale;
-  p.w_scale = w_scale;
+  p.perm = perm;
+  p.k = k;
+  p.x_scale = x_scale;
+  p.x_ld = x_ld;
+  p.s13 = s13;
+  p.s2 = s2;
   p.E = E;
   p.H = H;
   p.I = I;
   p.Pmax = Pmax;
-  p.n_blocks = mode == 1 ? (int)(I / 64) : (int)(H / 128);
-  p.h_t0 = h_terms ? h_terms[0] : nullptr;
-  p.h_t1 = h_terms ? h_terms[1] : nullptr;
-  p.h_t2 = h_terms ? h_terms[2] : nullptr;
+  p.h_t0 = h_terms[0];
+  p.h_t1 = h_terms[1];
+  p.h_t2 = h_terms[2];
   p.h_scale = h_scale;
   p.y = y;
+  p.done13 = done13;
   p.err = err;
+  if (E > kMaxE || H % 256 != 0) return cudaErrorInvalidValue;
+  const int64_t max_items = max_tiles * (H / 256 > I / 128 ? H / 256 : I / 128);
   const int64_t grid = max_items < sms ? max_items : sms;
   if (grid <= 0) return cudaSuccess;
-  cudaError_t e;
-  if (mode == 1) {
-    auto k = decode_mma_kernel<1, 2>;
-    if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DPipe<2>::SMEM)) != cudaSuccess) return e;
-    return launch_pdl(k, dim3((unsigned)grid), dim3(DTHREADS), DPipe<2>::SMEM, s, tm, p);
-  }
-  auto k = decode_mma_kernel<2, 3>;
-  if ((e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DPipe<3>::SMEM)) != cudaSuccess) return e;
-  return launch_pdl(k, dim3((unsigned)grid), dim3(DTHREADS), DPipe<3>::SMEM, s, tm, p);
+  cudaError_t e = cudaFuncSetAttribute(decode_ffn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)DSMEM);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_ffn_kernel, dim3((unsigned)grid), dim3(DTHREADS), DSMEM, s, maps, p);
 }
 
 }  // namespace fp8moe

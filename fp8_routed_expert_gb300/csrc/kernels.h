@@ -97,17 +97,45 @@ cudaError_t launch_grouped_gemm(int mode, const TmapSet &tm, const int32_t *offs
                                 const float *w_scale, int E, int64_t H, int64_t I, int64_t Pmax,
                                 uint8_t *const h_terms[3], float *h_scale, float *y, int *err,
                                 int64_t max_items, int sms, cudaStream_t s);
-// Tokens per tile of the tensor-core grouped GEMV (its MMA N).
-constexpr int kDecodeTileN = 16;
-// Tensor-core grouped GEMV for small batches (tiles of kDecodeTileN tokens,
-// tile_offsets counted in such tiles).  mode 1: gate/up + SwiGLU -> h as
-// three e4m3 terms with one power-of-two scale per (position, 64 outputs),
-// h_scale [I/64][Pmax]; mode 2: down -> f32 y.
-cudaError_t launch_decode_mma(int mode, const TmapSet &tm, const int32_t *offsets,
-                              const int32_t *tile_offsets, const float *act_scale,
-                              const float *w_scale, int E, int64_t H, int64_t I, int64_t Pmax,
-                              uint8_t *const h_terms[3], float *h_scale, float *y, int *err,
-                              int64_t max_items, int sms, cudaStream_t s);
+// Positions per tile of the tensor-core decode FFN.
+constexpr int kDecodeTileN = 32;
+// Tensor maps of the decode FFN: weights (W13 boxes of 128 rows, W2 boxes of
+// 256 rows), the token-major x terms (boxes of one row, for tile::gather4) and
+// the position-major h terms (boxes of kDecodeTileN rows).
+struct DecodeMaps {
+  CUtensorMap w13, w2;
+  CUtensorMap x[2];
+  CUtensorMap h[3];
+};
+// Gate/up + SwiGLU and down for small batches in one persistent launch
+// (tile_offsets counted in tiles of kDecodeTileN positions).  x terms are
+// token-major with scales x_scale[H/128][x_ld]; h is written as three e4m3
+// terms with one power-of-two scale per (position, 128 outputs), h_scale
+// [I/128][Pmax]; y f32 [Pmax, H].  done13 [max_tiles] must be zero on entry.
+// Needs H % 256 == 0.
+cudaError_t launch_decode_ffn(const DecodeMaps &maps, const int32_t *offsets,
+                              const int32_t *tile_offsets, const int32_t *perm, int k,
+                              const float *x_scale, int64_t x_ld, const float *s13, const float *s2,
+                              int E, int64_t H, int64_t I, int64_t Pmax, uint8_t *const h_terms[3],
+                              float *h_scale, float *y, int32_t *done13, int *err, int64_t max_tiles,
+                              int sms, cudaStream_t s);
+// Per-token activation terms (two e4m3 terms, one power-of-two scale per
+// (token, 128 columns)); the token-major operand of the decode FFN.
+cudaError_t launch_act_quant_tokens(const __nv_bfloat16 *x, int64_t T, int64_t H, uint8_t *a_hi,
+                                    uint8_t *a_lo, float *a_scale, int64_t a_ld, int sms,
+                                    cudaStream_t s);
+// T <= 64 on the tensor-core decode path: logits, per-token activation terms,
+// selection and the pair sort in one launch.  tickets: kSmallTicketInts ints,
+// zero between calls; counters [n_counters] are cleared.
+constexpr int kSmallTicketInts = 16;
+float route_small_gamma(int64_t H, int64_t E);
+cudaError_t launch_route_small(const __nv_bfloat16 *x, int64_t T, const float *W, const float *bias,
+                               int64_t E, int64_t H, int k, float *logits, float *wnorm, float *xss,
+                               uint8_t *a_hi, uint8_t *a_lo, float *a_scale, int64_t a_ld,
+                               int32_t *tickets, int32_t *counters, int n_counters, int32_t *idx,
+                               float *wts, int32_t *counts, int32_t *offsets, int32_t *perm,
+                               int32_t *inv, int32_t *active, int32_t *n_active,
+                               int32_t *tile_offsets, int tile_m, int *err, cudaStream_t s);
 cudaError_t launch_combine(const float *y, const int32_t *inv, const float *wts, int64_t T, int k,
                            int64_t H, __nv_bfloat16 *out, cudaStream_t s);
 

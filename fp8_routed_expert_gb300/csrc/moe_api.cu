@@ -42,8 +42,12 @@ struct moe_ctx {
   float *a_scale = nullptr;                      // [H/128][Pmax]
   float *h_scale = nullptr;                      // [I/128][Pmax] (GEMM) or [I/64][Pmax] (TCGEMV)
   TmapSet tm_gemm1, tm_gemm2;                    // activation terms (workspace) + last weights
-  TmapSet tm_dec1, tm_dec2;                      // the same operands in boxes of 16 positions
+  DecodeMaps dmaps;                              // tensor-core decode FFN operands
+  float *xss = nullptr;                          // per-(token, 128 columns) sums of squares of x
+  int32_t *tickets = nullptr;                    // small-batch routing tickets (0 between calls)
+  int32_t *done13 = nullptr;                     // decode FFN per-tile counters
   const void *tm_w13_ptr = nullptr, *tm_w2_ptr = nullptr;  // weights the maps in .b describe
+  const void *dmaps_w13 = nullptr, *dmaps_w2 = nullptr;    // weights dmaps describe
   int *err = nullptr;
   int path = MOE_PATH_AUTO;
   // last forward
@@ -127,15 +131,76 @@ void drain_timing(moe_ctx *c) {
     if (e_ != cudaSuccess) return MOE_ERR_CUDA; \
   } while (0)
 
+// The path a forward of T tokens takes.
+int resolve_path(const moe_ctx *c, int64_t T) {
+  int path = c->path != MOE_PATH_AUTO ? c->path : (T <= kGemvMaxT ? MOE_PATH_GEMV : MOE_PATH_GEMM);
+  // the tensor-core paths' down items are 256 output rows wide
+  if ((path == MOE_PATH_GEMM || path == MOE_PATH_TCGEMV) && c->cfg.hidden % 256 != 0) path = MOE_PATH_GEMV;
+  return path;
+}
+
 int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw,
                    const float *rb, const uint8_t *w13, const float *s13, const uint8_t *w2,
                    const float *s2, int k, __nv_bfloat16 *out, cudaStream_t s) {
   const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, I = c->cfg.inter;
   const int64_t P = T * k, Pm = c->cfg.max_tokens * c->cfg.max_top_k;
-  int path = c->path != MOE_PATH_AUTO ? c->path : (T <= kGemvMaxT ? MOE_PATH_GEMV : MOE_PATH_GEMM);
-  if (path == MOE_PATH_GEMM && H % 256 != 0) path = MOE_PATH_GEMV;  // GEMM2 tiles are 256 wide
+  const int path = resolve_path(c, T);
   const int64_t max_active = P < E ? P : E;
-  const int tile_m = path == MOE_PATH_TCGEMV ? kDecodeTileN : kTileM;
+  if (path == MOE_PATH_TCGEMV) {
+    const int64_t max_tiles = (P + kDecodeTileN - 1) / kDecodeTileN + max_active;
+    if (T <= kRouterWarpMaxT) {
+      Timed tm(c, MOE_K_ROUTE, s);
+      CUDA_TRY(launch_route_small(x, T, rw, rb, E, H, k, c->logits, c->wnorm, c->xss, c->a_hi,
+                                  c->a_lo, c->a_scale, Pm, c->tickets, c->done13, (int)max_tiles,
+                                  c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv, c->active,
+                                  c->n_active, c->tile_offsets, kDecodeTileN, c->err, s));
+    } else {
+      const int ks = router_k_split(T, E, H, c->sms);
+      {
+        Timed tm(c, MOE_K_ROUTER_LOGITS, s);
+        CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
+      }
+      {
+        Timed tm(c, MOE_K_ROUTER_SELECT, s);
+        CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks,
+                                      router_gamma(T, H, ks), c->idx, c->wts, c->err, s));
+      }
+      {
+        Timed tm(c, MOE_K_PERMUTE, s);
+        CUDA_TRY(launch_permute(c->idx, P, (int)E, kDecodeTileN, c->counts, c->offsets, c->perm,
+                                c->inv, c->active, c->n_active, c->tile_offsets, nullptr, c->done13,
+                                (int)max_tiles, c->err, s));
+      }
+      {
+        Timed tm(c, MOE_K_ACT_QUANT, s);
+        CUDA_TRY(launch_act_quant_tokens(x, T, H, c->a_hi, c->a_lo, c->a_scale, Pm, c->sms, s));
+      }
+    }
+    if (c->dmaps_w13 != w13) {
+      if (!encode_u8_tmap(&c->dmaps.w13, w13, H, E * 2 * I, 128)) return MOE_ERR_CUDA;
+      c->dmaps_w13 = w13;
+    }
+    if (c->dmaps_w2 != w2) {
+      if (!encode_u8_tmap(&c->dmaps.w2, w2, I, E * H, 256)) return MOE_ERR_CUDA;
+      c->dmaps_w2 = w2;
+    }
+    {
+      Timed tm(c, MOE_K_GATE_UP, s);
+      CUDA_TRY(launch_decode_ffn(c->dmaps, c->offsets, c->tile_offsets, c->perm, k, c->a_scale, Pm,
+                                 s13, s2, (int)E, H, I, Pm, c->h_t, c->h_scale, c->y, c->done13,
+                                 c->err, max_tiles, c->sms, s));
+    }
+    {
+      Timed tm(c, MOE_K_COMBINE, s);
+      CUDA_TRY(launch_combine(c->y, c->inv, c->wts, T, k, H, out, s));
+    }
+    c->last_T = T;
+    c->last_k = k;
+    c->last_stream = s;
+    if (c->timing && c->pending.size() > 16384) drain_timing(c);
+    return MOE_OK;
+  }
+  const int tile_m = kTileM;
   const int ks = router_k_split(T, E, H, c->sms);
   const float gamma = router_gamma(T, H, ks);
   if (T <= kRouterWarpMaxT) {
@@ -184,39 +249,22 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
       if (!encode_u8_tmap(&c->tm_gemm2.b, w2, I, E * H, 64)) return MOE_ERR_CUDA;
       c->tm_w2_ptr = w2;
     }
-    c->tm_dec1.b = c->tm_gemm1.b;
-    c->tm_dec2.b = c->tm_gemm2.b;
     const int64_t max_tiles = (P + tile_m - 1) / tile_m + max_active;
     {
       Timed tm(c, MOE_K_ACT_QUANT, s);
       CUDA_TRY(launch_act_quant(x, c->perm, P, k, H, Pm, c->a_hi, c->a_lo, c->a_scale, c->sms, s));
     }
-    if (path == MOE_PATH_TCGEMV) {
-      {
-        Timed tm(c, MOE_K_GATE_UP, s);
-        CUDA_TRY(launch_decode_mma(1, c->tm_dec1, c->offsets, c->tile_offsets, c->a_scale, s13,
+    {
+      Timed tm(c, MOE_K_GATE_UP, s);
+      CUDA_TRY(launch_grouped_gemm(1, c->tm_gemm1, c->offsets, c->tile_offsets, c->a_scale, s13,
                                    (int)E, H, I, Pm, c->h_t, c->h_scale, nullptr, c->err,
-                                   max_tiles * (I / 64), c->sms, s));
-      }
-      {
-        Timed tm(c, MOE_K_DOWN, s);
-        CUDA_TRY(launch_decode_mma(2, c->tm_dec2, c->offsets, c->tile_offsets, c->h_scale, s2,
+                                   max_tiles * (I / 128), c->sms, s));
+    }
+    {
+      Timed tm(c, MOE_K_DOWN, s);
+      CUDA_TRY(launch_grouped_gemm(2, c->tm_gemm2, c->offsets, c->tile_offsets, c->h_scale, s2,
                                    (int)E, H, I, Pm, nullptr, nullptr, c->y, c->err,
-                                   max_tiles * (H / 128), c->sms, s));
-      }
-    } else {
-      {
-        Timed tm(c, MOE_K_GATE_UP, s);
-        CUDA_TRY(launch_grouped_gemm(1, c->tm_gemm1, c->offsets, c->tile_offsets, c->a_scale, s13,
-                                     (int)E, H, I, Pm, c->h_t, c->h_scale, nullptr, c->err,
-                                     max_tiles * (I / 128), c->sms, s));
-      }
-      {
-        Timed tm(c, MOE_K_DOWN, s);
-        CUDA_TRY(launch_grouped_gemm(2, c->tm_gemm2, c->offsets, c->tile_offsets, c->h_scale, s2,
-                                     (int)E, H, I, Pm, nullptr, nullptr, c->y, c->err,
-                                     max_tiles * (H / 256), c->sms, s));
-      }
+                                   max_tiles * (H / 256), c->sms, s));
     }
   }
   {
@@ -310,6 +358,9 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->active, (size_t)E * 4},
       {(void **)&c->n_active, 16},
       {(void **)&c->ticket, 16},
+      {(void **)&c->tickets, (size_t)kSmallTicketInts * 4},
+      {(void **)&c->done13, (size_t)((Pm + kDecodeTileN - 1) / kDecodeTileN + E + 1) * 4},
+      {(void **)&c->xss, (size_t)(Tm * (H / 128)) * 4},
       {(void **)&c->xnorm, (size_t)Tm * 4},
       {(void **)&c->tile_offsets, (size_t)(E + 1) * 4},
       {(void **)&c->hmax, (size_t)Pm * 4},
@@ -352,12 +403,11 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       !encode_u8_tmap(&c->tm_gemm2.a[0], c->h_t[0], I, Pr, 128) ||
       !encode_u8_tmap(&c->tm_gemm2.a[1], c->h_t[1], I, Pr, 128) ||
       !encode_u8_tmap(&c->tm_gemm2.a[2], c->h_t[2], I, Pr, 128) ||
-      !encode_u8_tmap(&c->tm_dec1.a[0], c->a_hi, H, Pr, kDecodeTileN) ||
-      !encode_u8_tmap(&c->tm_dec1.a[1], c->a_lo, H, Pr, kDecodeTileN) ||
-      !encode_u8_tmap(&c->tm_dec1.a[2], c->a_lo, H, Pr, kDecodeTileN) ||
-      !encode_u8_tmap(&c->tm_dec2.a[0], c->h_t[0], I, Pr, kDecodeTileN) ||
-      !encode_u8_tmap(&c->tm_dec2.a[1], c->h_t[1], I, Pr, kDecodeTileN) ||
-      !encode_u8_tmap(&c->tm_dec2.a[2], c->h_t[2], I, Pr, kDecodeTileN)) {
+      !encode_u8_tmap(&c->dmaps.x[0], c->a_hi, H, Tm, 1) ||
+      !encode_u8_tmap(&c->dmaps.x[1], c->a_lo, H, Tm, 1) ||
+      !encode_u8_tmap(&c->dmaps.h[0], c->h_t[0], I, Pr, kDecodeTileN) ||
+      !encode_u8_tmap(&c->dmaps.h[1], c->h_t[1], I, Pr, kDecodeTileN) ||
+      !encode_u8_tmap(&c->dmaps.h[2], c->h_t[2], I, Pr, kDecodeTileN)) {
     cudaFree(c->ws);
     delete c;
     return MOE_ERR_CUDA;
@@ -446,6 +496,11 @@ int moe_set_path(moe_ctx *c, int path) {
     return MOE_ERR_ARG;
   c->path = path;
   return MOE_OK;
+}
+
+int moe_resolve_path(moe_ctx *c, int64_t T) {
+  if (c == nullptr || T < 0) return MOE_ERR_ARG;
+  return resolve_path(c, T);
 }
 
 int moe_set_timing(moe_ctx *c, int mask) {

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(1024) permute_kernel(
     int32_t *__restrict__ tile_offsets, uint32_t *__restrict__ pos_max,
     int32_t *__restrict__ counters, int n_counters, int *__restrict__ err) {
   extern __shared__ int sm[];
-  if ((int)threadIdx.x < n_counters) counters[threadIdx.x] = 0;
+  for (int i = threadIdx.x; i < n_counters; i += blockDim.x) counters[i] = 0;
   if (pos_max != nullptr)
     for (int64_t p = threadIdx.x; p < P; p += blockDim.x) pos_max[p] = 0u;
   SortOut o{counts, offsets, perm, inv, active, n_active, tile_offsets};

@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
         float amax = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          acc[j] = swiglu(acc[j], acc[64 + j]);
+          acc[j] = valid ? swiglu(acc[j], acc[64 + j]) : 0.f;  // rows past the segment hold garbage
           amax = fmaxf(amax, fabsf(acc[j]));
         }
         amax_x[half][r_in_tile] = amax;
@@ -276,6 +276,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
         named_bar_sync(1, 32 * NUM_EPI_WARPS);
         if (valid) {
           const int ex = e4m3_block_exponent(am);
+          const Pow2 down = pow2_factors(-ex);
           const int64_t off = row * p.I + (int64_t)c.nb * 128 + half * 64;
 #pragma unroll
           for (int j = 0; j < 64; j += 16) {
@@ -283,8 +284,8 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               uint32_t a[3], b[3];
-              e4m3_terms<3>(ldexpf(acc[j + 4 * m], -ex), ldexpf(acc[j + 4 * m + 1], -ex), a);
-              e4m3_terms<3>(ldexpf(acc[j + 4 * m + 2], -ex), ldexpf(acc[j + 4 * m + 3], -ex), b);
+              e4m3_terms<3>(down(acc[j + 4 * m]), down(acc[j + 4 * m + 1]), a);
+              e4m3_terms<3>(down(acc[j + 4 * m + 2]), down(acc[j + 4 * m + 3]), b);
               w0[m] = a[0] | (b[0] << 16);
               w1[m] = a[1] | (b[1] << 16);
               w2[m] = a[2] | (b[2] << 16);
@@ -321,38 +322,90 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
 }
 
 // ---------------------------------------------------------------- activation quantisation
-// Gathers the row of each position (token perm[pos] / k) and writes its two
-// e4m3 terms and the per-(row, 128-column block) power-of-two scale; a bf16
-// row block is held exactly by the two terms.  One warp per
-// (position, block): each lane handles 4 consecutive columns.
+// One bf16 row of H columns -> two e4m3 terms per 128-column block sharing
+// the block's power-of-two scale (a bf16 value is held exactly by the two
+// terms).  One warp per row: lane l takes 8 consecutive columns of every
+// 256-column span, so a half-warp covers one block (its amax is a 16-lane
+// reduction) and four spans' 16-byte loads are in flight at once.
+__device__ __forceinline__ void quant_row_2terms(const __nv_bfloat16 *__restrict__ src, int64_t H,
+                                                 uint8_t *__restrict__ dhi, uint8_t *__restrict__ dlo,
+                                                 float *__restrict__ scale, int64_t ld) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nsp = (H + 255) / 256;
+  for (int64_t sp0 = 0; sp0 < nsp; sp0 += 4) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t col = (sp0 + u) * 256 + lane * 8;
+      v[u] = (sp0 + u < nsp && col < H) ? __ldg(reinterpret_cast<const uint4 *>(src + col))
+                                        : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (sp0 + u >= nsp) break;  // uniform over the warp
+      const int64_t col = (sp0 + u) * 256 + lane * 8;
+      float f[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t w = u4_word(v[u], i);
+        f[2 * i] = bf16_bits_to_float(w & 0xffffu);
+        f[2 * i + 1] = bf16_bits_to_float(w >> 16);
+      }
+      float am = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const int ex = e4m3_block_exponent(am);
+      const Pow2 down = pow2_factors(-ex);
+      uint32_t hi[2], lo[2];
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        uint32_t a[2], b[2];
+        e4m3_terms<2>(down(f[4 * i]), down(f[4 * i + 1]), a);
+        e4m3_terms<2>(down(f[4 * i + 2]), down(f[4 * i + 3]), b);
+        hi[i] = a[0] | (b[0] << 16);
+        lo[i] = a[1] | (b[1] << 16);
+      }
+      if (col < H) {
+        *reinterpret_cast<uint2 *>(dhi + col) = make_uint2(hi[0], hi[1]);
+        *reinterpret_cast<uint2 *>(dlo + col) = make_uint2(lo[0], lo[1]);
+        if ((lane & 15) == 0) scale[(col / 128) * ld] = ldexpf(1.f, ex);
+      }
+    }
+  }
+}
+
+// Position rows: row pos is x of token perm[pos] / k (the expert-sorted
+// operand of the grouped GEMM); scales a_scale[kb * Pmax + pos].
 __global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__restrict__ x,
                                                         const int32_t *__restrict__ perm, int64_t P,
                                                         int k, int64_t H, int64_t Pmax,
                                                         uint8_t *__restrict__ a_hi,
                                                         uint8_t *__restrict__ a_lo,
                                                         float *__restrict__ a_scale) {
-  const int lane = threadIdx.x & 31;
-  const int64_t nkb = H / 128;
-  const int64_t n_items = P * nkb;
-  for (int64_t it = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; it < n_items;
-       it += ((int64_t)gridDim.x * blockDim.x) >> 5) {
-    const int64_t pos = it / nkb, kb = it % nkb;
-    const int64_t t = perm[pos] / k;
-    const int64_t col = kb * 128 + lane * 4;
-    const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(x + t * H + col));
-    const float v0 = bf16_bits_to_float(xv.x & 0xffffu), v1 = bf16_bits_to_float(xv.x >> 16);
-    const float v2 = bf16_bits_to_float(xv.y & 0xffffu), v3 = bf16_bits_to_float(xv.y >> 16);
-    float am = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
-    am = warp_max(am);
-    const int ex = e4m3_block_exponent(am);
-    const float s = ldexpf(1.f, ex);
-    uint32_t a[2], b[2];
-    e4m3_terms<2>(ldexpf(v0, -ex), ldexpf(v1, -ex), a);
-    e4m3_terms<2>(ldexpf(v2, -ex), ldexpf(v3, -ex), b);
-    *reinterpret_cast<uint32_t *>(a_hi + pos * H + col) = a[0] | (b[0] << 16);
-    *reinterpret_cast<uint32_t *>(a_lo + pos * H + col) = a[1] | (b[1] << 16);
-    if (lane == 0) a_scale[kb * Pmax + pos] = s;
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t pos = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; pos < P;
+       pos += ((int64_t)gridDim.x * blockDim.x) >> 5) {
+    const int64_t t = __ldg(perm + pos) / k;
+    quant_row_2terms(x + t * H, H, a_hi + pos * H, a_lo + pos * H, a_scale + pos, Pmax);
   }
+}
+
+// Token rows: the token-major operand of the decode FFN; scales
+// a_scale[kb * a_ld + t].
+__global__ void __launch_bounds__(256) act_quant_tokens_kernel(const __nv_bfloat16 *__restrict__ x,
+                                                               int64_t T, int64_t H,
+                                                               uint8_t *__restrict__ a_hi,
+                                                               uint8_t *__restrict__ a_lo,
+                                                               float *__restrict__ a_scale,
+                                                               int64_t a_ld) {
+  pdl_wait();
+  pdl_trigger();
+  for (int64_t t = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; t < T;
+       t += ((int64_t)gridDim.x * blockDim.x) >> 5)
+    quant_row_2terms(x + t * H, H, a_hi + t * H, a_lo + t * H, a_scale + t, a_ld);
 }
 
 // ---------------------------------------------------------------- tensor maps
@@ -389,13 +442,23 @@ bool encode_u8_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t row
 cudaError_t launch_act_quant(const __nv_bfloat16 *x, const int32_t *perm, int64_t P, int k,
                              int64_t H, int64_t Pmax, uint8_t *a_hi, uint8_t *a_lo, float *a_scale,
                              int sms, cudaStream_t s) {
-  const int64_t warps = P * (H / 128);
-  int64_t grid = (warps + 7) / 8;
+  int64_t grid = (P + 7) / 8;  // one warp per row
   const int64_t cap = (int64_t)sms * 8;
   if (grid > cap) grid = cap;
   if (grid <= 0) return cudaSuccess;
-  act_quant_kernel<<<(unsigned)grid, 256, 0, s>>>(x, perm, P, k, H, Pmax, a_hi, a_lo, a_scale);
-  return cudaGetLastError();
+  return launch_pdl(act_quant_kernel, dim3((unsigned)grid), dim3(256), 0, s, x, perm, P, k, H, Pmax,
+                    a_hi, a_lo, a_scale);
+}
+
+cudaError_t launch_act_quant_tokens(const __nv_bfloat16 *x, int64_t T, int64_t H, uint8_t *a_hi,
+                                    uint8_t *a_lo, float *a_scale, int64_t a_ld, int sms,
+                                    cudaStream_t s) {
+  int64_t grid = (T + 7) / 8;  // one warp per row
+  const int64_t cap = (int64_t)sms * 8;
+  if (grid > cap) grid = cap;
+  if (grid <= 0) return cudaSuccess;
+  return launch_pdl(act_quant_tokens_kernel, dim3((unsigned)grid), dim3(256), 0, s, x, T, H, a_hi,
+                    a_lo, a_scale, a_ld);
 }
 
 cudaError_t launch_grouped_gemm(int mode, const TmapSet &tm, const int32_t *offsets,

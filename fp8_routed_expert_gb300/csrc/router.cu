@@ -447,6 +447,167 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_decode_kernel(
   if (threadIdx.x == 0) *ticket = 0;
 }
 
+// ------------------------------------------------------------------ small-batch routing, tiled
+// One launch for T <= 64 (the tensor-core decode path).  The grid is
+// (expert blocks) x (token blocks of 8).  CTA (eb, tb) computes the logits of
+// EPC experts for the tb's tokens: WPE = 8 / EPC warps share one expert's row,
+// each over a contiguous range of 128-column chunks; a lane keeps four
+// partial sums (one per column of its 4-column slice), so the longest rounding
+// chain is nch_w + 2 (lane) + 5 (butterfly) + log2(WPE) (pairwise over warps)
+// + 1 (bias), nch_w = ceil(H / 128 / WPE).  The same CTAs split every token
+// row of the block into per-(token, 128-column chunk) units: two e4m3 terms
+// with one power-of-two scale (the tensor-core GEMV's activation operand,
+// token-major) and the chunk's sum of squares (for ||x_t||).
+// The last CTA of a token block (ticket per block) selects the top k of its
+// tokens, one warp per token; the last selecting CTA (second ticket) sorts
+// the pairs by expert and clears the work counters of the expert kernels.
+constexpr int kSmallTB = 8;  // tokens per token block
+
+struct RouteSmallArgs {
+  SelectArgs sel;             // logits [T][E], wnorm [E], idx, wts, err
+  int epc;                    // experts per CTA (1, 2, 4 or 8)
+  float *logits_w, *wnorm_w;
+  float *xss;                 // [T][H/128] per-chunk sums of squares
+  uint8_t *a_hi, *a_lo;       // [T, H] activation terms (token-major)
+  float *a_scale;             // [H/128][a_ld] power-of-two scales
+  int64_t a_ld;
+  int32_t *tickets;           // [kSmallTB + 1], 0 between calls
+  int32_t *counters;          // [n_counters] cleared for the expert kernels
+  int n_counters;
+  int tile_m;
+  SortOut so;
+};
+
+__global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(RouteSmallArgs r) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ float part_l[kRouteWarps][kSmallTB];
+  __shared__ float part_w[kRouteWarps];
+  __shared__ int s_last;
+  const SelectArgs &a = r.sel;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t E = a.E, H = a.H, T = a.T;
+  const int64_t nch = H / 128;
+  const int epc = r.epc, wpe = kRouteWarps / epc;
+  const int eb = blockIdx.x, tb = blockIdx.y, n_eb = gridDim.x, n_tb = gridDim.y;
+  const int64_t t0 = (int64_t)tb * kSmallTB;
+  const int nt = (int)((T - t0) < kSmallTB ? (T - t0) : kSmallTB);
+  pdl_trigger();
+
+  // ---- logits of EPC experts for the block's tokens
+  const int eslot = wid / wpe, part = wid % wpe;
+  const int64_t e = (int64_t)eb * epc + eslot;
+  const int64_t c_lo = nch * part / wpe, c_hi = nch * (part + 1) / wpe;
+  float acc[kSmallTB][4], wss[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < kSmallTB; ++j)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
+  if (e < E) {
+    const float *w = a.W + e * H;
+    for (int64_t c = c_lo; c < c_hi; ++c) {
+      const int64_t h = c * 128 + 4 * lane;
+      const float4 wv = __ldg(reinterpret_cast<const float4 *>(w + h));
+      wss[0] = fmaf(wv.x, wv.x, wss[0]);
+      wss[1] = fmaf(wv.y, wv.y, wss[1]);
+      wss[2] = fmaf(wv.z, wv.z, wss[2]);
+      wss[3] = fmaf(wv.w, wv.w, wss[3]);
+#pragma unroll
+      for (int j = 0; j < kSmallTB; ++j) {
+        if (j < nt) {
+          const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(a.x + (t0 + j) * H + h));
+          acc[j][0] = fmaf(bf16_bits_to_float(xv.x & 0xffffu), wv.x, acc[j][0]);
+          acc[j][1] = fmaf(bf16_bits_to_float(xv.x >> 16), wv.y, acc[j][1]);
+          acc[j][2] = fmaf(bf16_bits_to_float(xv.y & 0xffffu), wv.z, acc[j][2]);
+          acc[j][3] = fmaf(bf16_bits_to_float(xv.y >> 16), wv.w, acc[j][3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kSmallTB; ++j) {
+    const float v = warp_sum((acc[j][0] + acc[j][1]) + (acc[j][2] + acc[j][3]));
+    if (lane == 0) part_l[wid][j] = v;
+  }
+  {
+    const float v = warp_sum((wss[0] + wss[1]) + (wss[2] + wss[3]));
+    if (lane == 0) part_w[wid] = v;
+  }
+
+  // ---- activation units (token j of the block, chunk c), split over the
+  // warps of the token block's CTAs
+  {
+    const int64_t n_units = (int64_t)nt * nch;
+    for (int64_t u = (int64_t)eb * kRouteWarps + wid; u < n_units; u += (int64_t)n_eb * kRouteWarps) {
+      const int64_t t = t0 + u / nch, c = u % nch;
+      const int64_t col = c * 128 + 4 * lane;
+      const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(a.x + t * H + col));
+      const float v0 = bf16_bits_to_float(xv.x & 0xffffu), v1 = bf16_bits_to_float(xv.x >> 16);
+      const float v2 = bf16_bits_to_float(xv.y & 0xffffu), v3 = bf16_bits_to_float(xv.y >> 16);
+      const float am = warp_max(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
+      const float ss = warp_sum((v0 * v0 + v1 * v1) + (v2 * v2 + v3 * v3));
+      const int ex = e4m3_block_exponent(am);
+      const Pow2 down = pow2_factors(-ex);
+      uint32_t p[2], q[2];
+      e4m3_terms<2>(down(v0), down(v1), p);
+      e4m3_terms<2>(down(v2), down(v3), q);
+      *reinterpret_cast<uint32_t *>(r.a_hi + t * H + col) = p[0] | (q[0] << 16);
+      *reinterpret_cast<uint32_t *>(r.a_lo + t * H + col) = p[1] | (q[1] << 16);
+      if (lane == 0) {
+        r.a_scale[c * r.a_ld + t] = ldexpf(1.f, ex);
+        r.xss[t * nch + c] = ss;
+      }
+    }
+  }
+  __syncthreads();
+  // pairwise tree over the WPE warps of an expert, in a fixed order
+  if (threadIdx.x < epc * kSmallTB) {
+    const int es = threadIdx.x / kSmallTB, j = threadIdx.x % kSmallTB;
+    const int64_t ee = (int64_t)eb * epc + es;
+    float v[kRouteWarps];
+#pragma unroll
+    for (int q = 0; q < kRouteWarps; ++q) v[q] = q < wpe ? part_l[es * wpe + q][j] : 0.f;
+    for (int w = 1; w < wpe; w <<= 1)
+      for (int q = 0; q + w < wpe; q += 2 * w) v[q] = v[q] + v[q + w];
+    if (ee < E && j < nt) r.logits_w[(t0 + j) * E + ee] = v[0];
+    if (ee < E && j == 0 && tb == 0) {
+      float s = 0.f;
+      for (int q = 0; q < wpe; ++q) s += part_w[es * wpe + q];
+      r.wnorm_w[ee] = sqrtf(s);
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&r.tickets[tb], 1) == n_eb - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- selection: one warp per token of the block
+  double *lg64 = reinterpret_cast<double *>(smem_raw) + (size_t)wid * E;
+  float *lg = reinterpret_cast<float *>(smem_raw + (size_t)kRouteWarps * E * sizeof(double)) + (size_t)wid * 2 * E;
+  if (wid < nt) {
+    const int64_t t = t0 + wid;
+    float ss = 0.f;
+    for (int64_t c = lane; c < nch; c += 32) ss += __ldcg(r.xss + t * nch + c);
+    const float xn = sqrtf(warp_sum(ss));
+    select_token(a, t, xn, lg, lg + E, lg64);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    r.tickets[tb] = 0;
+    s_last = atomicAdd(&r.tickets[kSmallTB], 1) == n_tb - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  // ---- stable sort of the pairs by expert; clear the expert kernels' counters
+  for (int i = threadIdx.x; i < r.n_counters; i += blockDim.x) r.counters[i] = 0;
+  cta_counting_sort<kRouteWarps>(a.idx, T * a.k, (int)E, r.tile_m, r.so, reinterpret_cast<int *>(smem_raw), a.err);
+  if (threadIdx.x == 0) r.tickets[kSmallTB] = 0;
+}
+
 // f16 copies of every token (the GEMV path above the fused-routing size).
 __global__ void __launch_bounds__(128) x_to_f16_kernel(const __nv_bfloat16 *__restrict__ x, int64_t T,
                                                        int64_t H, __half *__restrict__ x16,
@@ -642,6 +803,49 @@ cudaError_t launch_route_decode(const __nv_bfloat16 *x, int64_t T, const float *
     if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess) return e;
     kern<<<(unsigned)E, 32 * kRouteWarps, smem, s>>>(a, logits, wnorm, xnorm, x16, xscale, ticket, tile_m, so, pos_max);
   }
+  return cudaGetLastError();
+}
+
+int route_small_epc(int64_t E) { return E <= 128 ? 1 : (E <= 256 ? 2 : (E <= 512 ? 4 : 8)); }
+
+float route_small_gamma(int64_t H, int64_t E) {
+  const int wpe = kRouteWarps / route_small_epc(E);
+  int lg = 0;
+  while ((1 << lg) < wpe) ++lg;
+  const int64_t nch_w = (H / 128 + wpe - 1) / wpe;
+  const double u = 1.0 / 16777216.0;  // 2^-24
+  const double d = (double)(nch_w + 2 + 5 + lg + 1);
+  const double g = d * u / (1.0 - d * u);
+  return nextafterf((float)(g * (1.0 + 1e-6)), INFINITY);
+}
+
+cudaError_t launch_route_small(const __nv_bfloat16 *x, int64_t T, const float *W, const float *bias,
+                               int64_t E, int64_t H, int k, float *logits, float *wnorm, float *xss,
+                               uint8_t *a_hi, uint8_t *a_lo, float *a_scale, int64_t a_ld,
+                               int32_t *tickets, int32_t *counters, int n_counters, int32_t *idx,
+                               float *wts, int32_t *counts, int32_t *offsets, int32_t *perm,
+                               int32_t *inv, int32_t *active, int32_t *n_active,
+                               int32_t *tile_offsets, int tile_m, int *err, cudaStream_t s) {
+  RouteSmallArgs r;
+  r.sel = select_args(x, T, W, bias, E, H, k, logits, 1, wnorm, route_small_gamma(H, E), idx, wts, err);
+  r.epc = route_small_epc(E);
+  r.logits_w = logits;
+  r.wnorm_w = wnorm;
+  r.xss = xss;
+  r.a_hi = a_hi;
+  r.a_lo = a_lo;
+  r.a_scale = a_scale;
+  r.a_ld = a_ld;
+  r.tickets = tickets;
+  r.counters = counters;
+  r.n_counters = n_counters;
+  r.tile_m = tile_m;
+  r.so = SortOut{counts, offsets, perm, inv, active, n_active, tile_offsets};
+  const size_t smem = route_decode_smem(E);
+  cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((unsigned)((E + r.epc - 1) / r.epc), (unsigned)((T + kSmallTB - 1) / kSmallTB));
+  route_small_kernel<<<grid, 32 * kRouteWarps, smem, s>>>(r);
   return cudaGetLastError();
 }
 

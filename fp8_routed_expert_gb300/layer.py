@@ -114,6 +114,13 @@ class MoELayer:
     def set_path(self, path: str) -> None:
         check(lib().moe_set_path(self._h, PATHS[path]), "moe_set_path")
 
+    def resolved_path(self, T: int) -> str:
+        """Name of the path a forward of T tokens takes ("gemv", "gemm" or "tcgemv")."""
+        code = lib().moe_resolve_path(self._h, T)
+        if code < 0:
+            check(code, "moe_resolve_path")
+        return {v: k for k, v in PATHS.items()}[code]
+
     def set_timing(self, kernels=()) -> None:
         """Time the named kernels (an iterable of KERNELS keys, or "all"); () turns timing off."""
         names = KERNELS if kernels == "all" else kernels

@@ -157,6 +157,9 @@ const char *moe_strerror(int code);
 #define MOE_PATH_GEMM 2
 #define MOE_PATH_TCGEMV 3
 int moe_set_path(moe_ctx *ctx, int path);
+/* moe_resolve_path - the MOE_PATH_* (not AUTO) a forward of T tokens would
+ * take on this context; MOE_ERR_ARG for a NULL context or T < 0. */
+int moe_resolve_path(moe_ctx *ctx, int64_t T);
 
 /*
  * Kernel timing.  moe_set_timing(ctx, mask) records CUDA events around each

@@ -54,6 +54,7 @@ def test_null_arguments(L):
                                None) == moe.C["MOE_ERR_ARG"]
     assert L.moe_status(None) == moe.C["MOE_ERR_ARG"]
     assert L.moe_set_path(None, 0) == moe.C["MOE_ERR_ARG"]
+    assert L.moe_resolve_path(None, 1) == moe.C["MOE_ERR_ARG"]
 
 
 def test_error_strings(L):
