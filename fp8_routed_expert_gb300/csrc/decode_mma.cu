@@ -5,43 +5,47 @@
 // The time of a decode step goes to moving expert weight bytes (DeepSeek-
 // V4.1-Flash post, "Bytes per token decide everything"), so the kernel is
 // built to stream them: each item's 256 weight rows are the MMA's N = 256
-// operand, loaded by TMA in 32 KiB stages (one or two boxes) and multiplied
-// in shared memory by tcgen05.mma without any per-byte instruction on the SM;
-// one M64 x N256 x K32 MMA covers 8 KiB of weights.
+// operand, loaded by TMA in 32 KiB stages and multiplied in shared memory by
+// tcgen05.mma without any per-byte instruction on the SM.
 //
 // Operands.  B = e4m3 weight rows (one f32 scale per 128 x 128 block).
-// A = the tile's activations as e4m3 terms that share one power-of-two scale
-// per (row, 128-column block); each term is its own MMA into the same TMEM
-// accumulator, so the terms add up in the tensor core.  Gate/up reads x (two
-// terms hold a bf16 value exactly), token-major, gathered four rows at a time
-// by TMA (tile::gather4) from the tile's token list into the first four rows of
-// each 8-row 128-byte-swizzle atom: position j of the tile is A row
-// 8 (j / 4) + j % 4 (a tile holds 32 positions; the other rows are never read
-// back).  Down reads h (three terms, about 12 bits) in position order, 32
-// rows per term.  Every 128-wide K block is accumulated in one of two TMEM
-// buffers and promoted in f32 registers as partial * s_w[row block, kb] *
-// s_act[row, kb] (dragon.c §8 "Round 3": the block scale is folded out of the
-// inner product), while the MMA fills the other buffer.
+// A = the tile's activations (up to 16 positions) as e4m3 terms that share
+// one power-of-two scale per (row, 128-column block), stacked along M so
+// that one M64 x N256 x K32 MMA covers every term:
+//   gate/up: x in two terms (exact for bf16), token-major, gathered four rows
+//     at a time by TMA (tile::gather4) into the first four rows of 8-row
+//     128-byte-swizzle atoms: term t, position j is A row 32 t + 8 (j / 4) +
+//     j % 4 (the other rows are never read back);
+//   down: h in three terms (about 12 bits), position order: term t, position
+//     j is A row 16 t + j.
+// Every 128-wide K block is accumulated in one of two TMEM buffers and
+// promoted in f32 registers as partial * s_w[row block, kb] * s_act[row, kb]
+// (dragon.c §8 "Round 3": the block scale is folded out of the inner
+// product) while the MMA fills the other buffer; at the end of an item the
+// terms' rows are added through shared memory.
 //
 // Phases.  CTA c owns a contiguous share of the gate/up items and one of the
 // down items (counted from the other end of the list, so that the CTAs with
 // more gate/up work get less down work) and runs them in that order.  A down
 // item needs h of its tile, i.e. every gate/up item of the tile (possibly
 // other CTAs'): each CTA publishes its gate/up items on per-tile counters when
-// it has finished them, and the activation producer of a down item waits
-// (bounded) until the tile's counter is complete.  The weights do not depend
-// on h, so the weight producer runs ahead across the phase boundary and HBM
-// stays busy.  All CTAs are resident (one per SM, grid <= SMs) and every
-// gate/up item precedes every down item in each CTA's order, so the waits end.
+// it has finished them, and the activation producer and the epilogue of a
+// down item wait (bounded) until the tile's counter is complete.  The weights
+// do not depend on h, so the weight producer runs ahead across the phase
+// boundary and HBM stays busy.  All CTAs are resident (one per SM, grid <=
+// SMs) and every gate/up item precedes every down item in each CTA's order,
+// so the waits end.
 //
 // Accumulator layout (M = 64, one CTA): row 16 q + l sits in TMEM lane
 // 32 q + l for l < 16.  The epilogue reads it with tcgen05.ld.16x64b: in the
 // warp of lane quarter q, thread t holds row 16 q + (t >> 2) + 8 (t & 1) and,
 // of every 64 columns, those with parity (t >> 1) & 1, so the two threads of
-// a row (t and t ^ 2) split its columns and every thread carries data.
+// a row (t and t ^ 2) split its columns.
 // Warps: 0 weight TMA; 1 TMEM allocation and MMA issue; 2 activation TMA;
-// 4..7 promotion and epilogue (warp w reads lane quarter w % 4); 3 idle.
-// Every mbarrier wait and the counter wait are bounded by wall-clock time.
+// 4..11 promotion and epilogue (warp w reads lane quarter w % 4 and column
+// half (w - 4) / 4); 3 idle.  The producer and MMA loops are warp-uniform
+// (lane 0 issues).  Every mbarrier wait and counter wait is bounded by
+// wall-clock time.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100_ptx.cuh"
@@ -51,25 +55,24 @@ using namespace sm100;
 
 namespace {
 
-constexpr int BM = 64;                 // MMA M: A rows (positions, per term)
-constexpr int TP = kDecodeTileN;       // positions per tile (32)
+constexpr int BM = 64;                 // MMA M: stacked activation rows
+constexpr int TP = kDecodeTileN;       // positions per tile (16)
 constexpr int BN = 256;                // weight rows per item
 constexpr int BK = 128;                // K per stage
-constexpr int AX_TERM = 8 * 1024;      // x term: 8 atoms of 8 rows, 4 filled
-constexpr int AH_TERM = TP * BK;       // h term: 32 rows (4 KiB)
-constexpr int A_REGION = 2 * AX_TERM;  // 16 KiB (also holds 3 h terms + the 4 KiB read past the last)
+constexpr int A_BYTES = BM * BK;       // 8 KiB
 constexpr int B_BYTES = BN * BK;       // 32 KiB
-constexpr int STAGE = A_REGION + B_BYTES;
-constexpr int STAGES = 4;
+constexpr int STAGE = A_BYTES + B_BYTES;
+constexpr int STAGES = 5;
 constexpr uint32_t TMEM_COLS = 512;    // two 256-column accumulators
-constexpr int EPI_THREADS = 128;       // warps 4..7
+constexpr int EPI_WARPS = 8;
+constexpr int EPI_THREADS = 32 * EPI_WARPS;
+constexpr int XCH_FLOATS = 2048;       // 8 KiB exchange buffer
 constexpr int kMaxE = 1024;
-constexpr int DTHREADS = 32 * 8;
-constexpr size_t DSMEM = (size_t)STAGES * STAGE + 1024;
+constexpr int DTHREADS = 32 * 12;
+constexpr size_t DSMEM = (size_t)STAGES * STAGE + XCH_FLOATS * 4 + 1024;
 constexpr uint64_t DWAIT_NS = 2000000000ull;
 
-static_assert(TP == 32, "tile of 32 positions: 8 gather atoms of 4 rows");
-static_assert(3 * AH_TERM + (BM - TP) * BK <= A_REGION + B_BYTES, "h MMA reads stay in the stage");
+static_assert(TP == 16, "tiles of 16 positions: 4 gather atoms per x term, 16 rows per h term");
 
 struct FfnArgs {
   const int32_t *offsets, *tile_offsets;  // tile offsets in units of TP-position tiles
@@ -90,7 +93,7 @@ struct FfnArgs {
 struct DItem {
   int e, nb;
   int64_t tile;       // global tile index
-  int64_t p0, p_end;  // first position of the tile, end of the expert's segment
+  int64_t p0;         // first position of the tile
   int nvalid;         // positions of this tile (1..TP)
 };
 
@@ -106,8 +109,7 @@ __device__ __forceinline__ DItem ditem(const int *toff, const int *off, int E, i
   }
   c.e = lo;
   c.p0 = off[lo] + (c.tile - toff[lo]) * TP;
-  c.p_end = off[lo + 1];
-  const int64_t n = c.p_end - c.p0;
+  const int64_t n = off[lo + 1] - c.p0;
   c.nvalid = (int)(n < TP ? n : TP);
   return c;
 }
@@ -150,6 +152,21 @@ __device__ __forceinline__ void fail(volatile int *abort_flag, int *err) {
   set_error(err, DEV_ERR_TIMEOUT);
 }
 
+// Lane 0 waits (bounded) until the tile's gate/up items are all published;
+// the outcome is broadcast to the warp.
+__device__ __forceinline__ bool wait_tile(const int32_t *done13, int64_t tile, int need,
+                                          volatile int *abort_flag) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) {
+    const uint64_t t0 = global_timer_ns();
+    while (ld_acquire(done13 + tile) < need) {
+      if (*abort_flag || global_timer_ns() - t0 > DWAIT_NS) { ok = false; break; }
+    }
+    fence_proxy_async_global();
+  }
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 // 16 lanes x 64 columns (tcgen05.ld.16x64b.x32, no wait): value i of thread
 // t is lane (t >> 2) + 8 (t & 1), column 2 i + ((t >> 1) & 1).
 __device__ __forceinline__ void tmem_ld16x64(uint32_t taddr, float *v) {
@@ -175,10 +192,12 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
   __shared__ int s_toff[kMaxE + 1], s_off[kMaxE + 1];
   __shared__ uint32_t tmem_base_sh;
   __shared__ volatile int abort_flag;
-  __shared__ int32_t s_rows[TP];  // token rows of the activation producer's current tile
+  __shared__ int32_t s_rows[TP];   // token rows of the activation producer's current tile
+  __shared__ float s_amax[2][TP];  // per (column half, position) |h| maxima
 
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  float *xch = reinterpret_cast<float *>(smem + (size_t)STAGES * STAGE);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t nkb1 = p.H / BK, nkb2 = p.I / BK;
 
@@ -190,7 +209,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], EPI_THREADS / 32);
+      mbar_init(&tempty[b], EPI_WARPS);
     }
     abort_flag = 0;
     fence_mbar_init();
@@ -226,7 +245,6 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
 
   if (warp == 0) {
     // ---------------------------------------------------------------- weight TMA
-    // The whole warp walks the stages (waits are warp-uniform); lane 0 issues.
     if (lane == 0) {
       prefetch_tmap(&tm.w13);
       prefetch_tmap(&tm.w2);
@@ -241,14 +259,13 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
                             : (int64_t)c.e * 2 * p.I + (int64_t)c.nb * 128;  // 128 gate rows
       const int64_t nkb = dn ? nkb2 : nkb1;
       for (int64_t kb = 0; kb < nkb; ++kb) {
-        // every lane waits; the outcome is made warp-uniform
         if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag, DWAIT_NS))) {
           if (lane == 0) fail(&abort_flag, p.err);
           run = false;
           break;
         }
         if (lane == 0) {
-          uint8_t *sb = smem + (size_t)stage * STAGE + A_REGION;
+          uint8_t *sb = smem + (size_t)stage * STAGE + A_BYTES;
           mbar_arrive_expect_tx(&full_b[stage], B_BYTES);
           const int32_t kx = (int32_t)(kb * BK);
           if (dn) {
@@ -276,33 +293,18 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
       const bool dn = plan.down(q);
       const DItem c = ditem(s_toff, s_off, p.E, plan.nblocks(q), plan.item(q));
       const int64_t nkb = dn ? nkb2 : nkb1;
-      int32_t tok = 0;
       if (!dn) {
-        // token of each of the tile's positions (lane j); padding positions
-        // repeat the tile's first token and their rows are never read back
-        tok = __ldg(p.perm + c.p0 + (lane < c.nvalid ? lane : 0)) / p.k;
-      } else {
-        // down: wait until every gate/up item of this tile has published h
-        bool ok = true;
-        if (lane == 0) {
-          const uint64_t t0 = global_timer_ns();
-          while (ld_acquire(p.done13 + c.tile) < plan.nb1) {
-            if (abort_flag || global_timer_ns() - t0 > DWAIT_NS) { ok = false; break; }
-          }
-          fence_proxy_async_global();
-        }
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) {
-          if (lane == 0) fail(&abort_flag, p.err);
-          break;
-        }
+        // token of each of the tile's positions; padding positions repeat
+        // the tile's first token and their rows are never read back
+        __syncwarp();
+        if (lane < TP) s_rows[lane] = __ldg(p.perm + c.p0 + (lane < c.nvalid ? lane : 0)) / p.k;
+        __syncwarp();
+      } else if (!wait_tile(p.done13, c.tile, plan.nb1, &abort_flag)) {
+        if (lane == 0) fail(&abort_flag, p.err);
+        break;
       }
       const int n_atoms = (c.nvalid + 3) / 4;
-      __syncwarp();
-      s_rows[lane] = tok;
-      __syncwarp();
       for (int64_t kb = 0; kb < nkb; ++kb) {
-        // every lane waits; the outcome is made warp-uniform
         if (!__all_sync(0xffffffffu, mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag, DWAIT_NS))) {
           if (lane == 0) fail(&abort_flag, p.err);
           run = false;
@@ -314,14 +316,14 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
           if (!dn) {
             mbar_arrive_expect_tx(&full_a[stage], (uint32_t)(2 * n_atoms * 512));
             for (int t = 0; t < 2; ++t)
-              for (int g = 0; g < n_atoms; ++g)  // atom g of term t: 1024-byte aligned
-                tma_gather4(sa + t * AX_TERM + g * 1024, &tm.x[t], kx, s_rows[4 * g], s_rows[4 * g + 1],
+              for (int g = 0; g < n_atoms; ++g)  // atom 4 t + g: 1024-byte aligned
+                tma_gather4(sa + (4 * t + g) * 1024, &tm.x[t], kx, s_rows[4 * g], s_rows[4 * g + 1],
                             s_rows[4 * g + 2], s_rows[4 * g + 3], &full_a[stage]);
           } else {
-            mbar_arrive_expect_tx(&full_a[stage], 3 * AH_TERM);
+            mbar_arrive_expect_tx(&full_a[stage], 3 * TP * BK);
 #pragma unroll
             for (int t = 0; t < 3; ++t)
-              tma_load_2d(sa + t * AH_TERM, &tm.h[t], kx, (int32_t)c.p0, &full_a[stage]);
+              tma_load_2d(sa + t * TP * BK, &tm.h[t], kx, (int32_t)c.p0, &full_a[stage]);
           }
         }
         __syncwarp();
@@ -330,14 +332,12 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA
-    // The whole warp walks the stages (waits are warp-uniform); lane 0 issues.
     const uint32_t idesc = idesc_e4m3_f32(BM, BN);
     int stage = 0, buf = 0;
     uint32_t phase = 0, bphase = 0;
     bool run = true;
     for (int64_t q = 0; q < nq && run; ++q) {
-      const bool dn = plan.down(q);
-      const int64_t nkb = dn ? nkb2 : nkb1;
+      const int64_t nkb = plan.down(q) ? nkb2 : nkb1;
       for (int64_t kb = 0; kb < nkb; ++kb) {
         const bool ready = mbar_wait(&full_b[stage], phase, &abort_flag, DWAIT_NS) &&
                            mbar_wait(&full_a[stage], phase, &abort_flag, DWAIT_NS) &&
@@ -350,24 +350,11 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
         tc_fence_after();
         if (lane == 0) {
           const uint32_t a = smem_u32(smem + (size_t)stage * STAGE);
-          const uint64_t bdesc = sw128_kmajor_desc(a + A_REGION);
-          const uint64_t adesc = sw128_kmajor_desc(a);
+          const uint64_t adesc = sw128_kmajor_desc(a), bdesc = sw128_kmajor_desc(a + A_BYTES);
           const uint32_t d = tmem + (uint32_t)(buf * BN);
-          if (dn) {
 #pragma unroll
-            for (int kk = 0; kk < BK / 32; ++kk)
-#pragma unroll
-              for (int t = 0; t < 3; ++t)  // the descriptor's address field counts 16 bytes
-                mma_f8f6f4(d, adesc + (uint64_t)((t * AH_TERM + kk * 32) >> 4), bdesc + (uint64_t)(kk * 2),
-                           idesc, (kk > 0 || t > 0) ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < BK / 32; ++kk)
-#pragma unroll
-              for (int t = 0; t < 2; ++t)
-                mma_f8f6f4(d, adesc + (uint64_t)((t * AX_TERM + kk * 32) >> 4), bdesc + (uint64_t)(kk * 2),
-                           idesc, (kk > 0 || t > 0) ? 1u : 0u);
-          }
+          for (int kk = 0; kk < BK / 32; ++kk)  // the descriptors' address field counts 16 bytes
+            mma_f8f6f4(d, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), idesc, kk > 0 ? 1u : 0u);
           mma_commit(&empty_bar[stage]);
           mma_commit(&tfull[buf]);
         }
@@ -379,9 +366,10 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
     }
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- promotion + epilogue
-    const int quarter = warp & 3;                             // TMEM lanes 32 quarter .. + 15
-    const int row = quarter * 16 + (lane >> 2) + 8 * (lane & 1);  // accumulator (A) row
-    const int par = (lane >> 1) & 1;                          // parity of this thread's columns
+    const int quarter = warp & 3;      // TMEM lanes 32 quarter .. + 15
+    const int half = (warp - 4) >> 2;  // column half of the 256-wide item
+    const int rq = (lane >> 2) + 8 * (lane & 1);  // row within the quarter
+    const int par = (lane >> 1) & 1;   // parity of this thread's columns
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     int buf = 0;
     uint32_t bphase = 0;
@@ -390,9 +378,18 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
       const bool dn = plan.down(q);
       const DItem c = ditem(s_toff, s_off, p.E, plan.nblocks(q), plan.item(q));
       const int64_t nkb = dn ? nkb2 : nkb1;
-      // position of this thread's row: x rows fill 4 of every 8 (gather atoms)
-      const int j = dn ? row : (row >> 3) * 4 + (row & 7);
-      const bool valid = dn ? (row < c.nvalid) : ((row & 7) < 4 && j < c.nvalid);
+      // this thread's row: position j of term (quarter >> 1) (gate/up) or
+      // of term quarter (down)
+      int j;
+      bool has_row;
+      if (!dn) {
+        j = 8 * (quarter & 1) + 4 * (lane & 1) + (lane >> 2);
+        has_row = lane < 16;  // rows 4..7 of each gather atom are never filled
+      } else {
+        j = rq;
+        has_row = quarter < 3;
+      }
+      const bool valid = has_row && j < c.nvalid;
       const int64_t pos = c.p0 + (valid ? j : 0);
       const float *sa_p;
       int64_t sa_ld;
@@ -402,35 +399,31 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
       } else {
         // h and its scales are written in this launch by other CTAs: acquire
         // the tile's counter before reading them, and read them coherently
-        bool dep = true;
-        if (lane == 0) {
-          const uint64_t t0 = global_timer_ns();
-          while (ld_acquire(p.done13 + c.tile) < plan.nb1) {
-            if (abort_flag || global_timer_ns() - t0 > DWAIT_NS) { dep = false; break; }
-          }
-        }
-        if (__shfl_sync(0xffffffffu, dep ? 1 : 0, 0) == 0) fail(&abort_flag, p.err);
+        if (!wait_tile(p.done13, c.tile, plan.nb1, &abort_flag)) fail(&abort_flag, p.err);
         sa_p = p.h_scale + pos;
         sa_ld = p.Pmax;
       }
-      // x scales come from the previous kernel (read-only path); h scales
-      // from this one (L2, coherent)
-      auto ld_scale = [&](const float *a) -> float { return dn ? __ldcg(a) : __ldg(a); };
-      // weight scale rows of columns [0, 128) and [128, 256): gate / up rows
-      // (gate/up) or the item's two 128-row blocks (down)
+      // weight scale rows of this half's two 64-column chunks: gate / up
+      // rows (gate/up) or the half's 128-row block (down)
       const float *wsc = dn ? p.s2 + (int64_t)c.e * (p.H / 128) * nkb2
                             : p.s13 + (int64_t)c.e * (2 * p.I / 128) * nkb1;
-      const int64_t wb0 = dn ? 2 * (int64_t)c.nb : c.nb;
-      const int64_t wb1 = dn ? 2 * (int64_t)c.nb + 1 : p.I / 128 + c.nb;
-      // acc[32 ch + i] = column 64 ch + 2 i + par
-      float acc[128];
+      const int64_t wb0 = dn ? 2 * (int64_t)c.nb + half : c.nb;
+      const int64_t wb1 = dn ? 2 * (int64_t)c.nb + half : p.I / 128 + c.nb;
+      // columns of this half's two chunks
+      const uint32_t col0 = dn ? 128u * half : 64u * half;
+      const uint32_t col1 = dn ? 128u * half + 64u : 128u + 64u * half;
+      auto ld_sa = [&](int64_t kb) -> float {
+        return dn ? __ldcg(sa_p + kb * sa_ld) : __ldg(sa_p + kb * sa_ld);
+      };
+      // acc[i] = column col0 + 2 i + par, acc[32 + i] = column col1 + 2 i + par
+      float acc[64];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.f;
-      float sa_n = ld_scale(sa_p), s0_n = __ldg(wsc + wb0 * nkb), s1_n = __ldg(wsc + wb1 * nkb);
+      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+      float sa_n = ld_sa(0), s0_n = __ldg(wsc + wb0 * nkb), s1_n = __ldg(wsc + wb1 * nkb);
       for (int64_t kb = 0; kb < nkb; ++kb) {
         const float sa = sa_n, c0 = sa * s0_n, c1 = sa * s1_n;
         if (kb + 1 < nkb) {  // next block's scales, in flight while this one is promoted
-          sa_n = ld_scale(sa_p + (kb + 1) * sa_ld);
+          sa_n = ld_sa(kb + 1);
           s0_n = __ldg(wsc + wb0 * nkb + kb + 1);
           s1_n = __ldg(wsc + wb1 * nkb + kb + 1);
         }
@@ -441,14 +434,16 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
         }
         tc_fence_after();
         const uint32_t tb = t_lane + (uint32_t)(buf * BN);
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
+        {
           float v[32];
-          tmem_ld16x64(tb + (uint32_t)(64 * ch), v);
+          tmem_ld16x64(tb + col0, v);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          const float sc = ch < 2 ? c0 : c1;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[ch * 32 + i] = fmaf(v[i], sc, acc[ch * 32 + i]);
+          for (int i = 0; i < 32; ++i) acc[i] = fmaf(v[i], c0, acc[i]);
+          tmem_ld16x64(tb + col1, v);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(v[i], c1, acc[32 + i]);
         }
         tc_fence_before();
         __syncwarp();
@@ -456,65 +451,87 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
         buf ^= 1;
         if (buf == 0) bphase ^= 1u;
       }
-      // all four epilogue warps agree before the next phase's shared state
+      // all epilogue warps agree before the shared buffers are touched
       ok = named_bar_and(1, EPI_THREADS, ok);
       if (!ok) break;
+      // add the terms' rows into term 0's warps through shared memory:
+      // gate/up: quarter 2 -> 0 and 3 -> 1; down: quarters 1 and 2 -> 0.
+      // Four rounds of 16 values per thread; each round rotates acc[] by 16.
+      {
+        const int src = dn ? (quarter == 1 ? 0 : (quarter == 2 ? 1 : -1)) : (quarter >= 2 ? quarter - 2 : -1);
+#pragma unroll 1
+        for (int r = 0; r < 4; ++r) {
+          if (src >= 0) {
+            float *d = xch + (((half * 2 + src) * 32 + lane) * 16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) d[i] = acc[i];
+          }
+          named_bar_sync(1, EPI_THREADS);
+          if (!dn && quarter < 2) {
+            const float *s = xch + (((half * 2 + quarter) * 32 + lane) * 16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] += s[i];
+          } else if (dn && quarter == 0) {
+            const float *s0 = xch + (((half * 2 + 0) * 32 + lane) * 16);
+            const float *s1 = xch + (((half * 2 + 1) * 32 + lane) * 16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] += s0[i] + s1[i];
+          }
+          named_bar_sync(1, EPI_THREADS);
+          float t16[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) t16[i] = acc[i];
+#pragma unroll
+          for (int i = 0; i < 48; ++i) acc[i] = acc[i + 16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[48 + i] = t16[i];
+        }
+      }
+      const bool owner = dn ? (quarter == 0) : (quarter < 2);  // warps holding the summed rows
       if (!dn) {
-        // h = silu(gate) * up: gate column 64 ch + 2 i + par pairs with up
-        // column 128 + (the same); h output o = 64 ch + 2 i + par, ch in {0, 1}.
-        // The tail runs once per item, so its code is kept short (it is
-        // fetched cold once per CTA): loops over small unrolled bodies that
-        // rotate the accumulator registers instead of indexing them.
+        // h = silu(gate) * up for outputs o = 64 half + 2 i + par (i < 32);
+        // one power-of-two scale per (position, 128 outputs) from both
+        // parities (lane ^ 2) and both halves (shared memory)
         float amax = 0.f;
-#pragma unroll 1
-        for (int k = 0; k < 4; ++k) {  // 16 outputs per pass; afterwards acc[0..63] = h in order
-          float hv[16];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            hv[i] = valid ? swiglu(acc[i], acc[64 + i]) : 0.f;  // rows without a position hold garbage
-            amax = fmaxf(amax, fabsf(hv[i]));
-          }
-#pragma unroll
-          for (int i = 0; i < 48; ++i) {
-            acc[i] = acc[i + 16];
-            acc[64 + i] = acc[80 + i];
-          }
-#pragma unroll
-          for (int i = 0; i < 16; ++i) acc[48 + i] = hv[i];
+        for (int i = 0; i < 32; ++i) {
+          acc[i] = (owner && valid) ? swiglu(acc[i], acc[32 + i]) : 0.f;
+          amax = fmaxf(amax, fabsf(acc[i]));
         }
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));  // the row's other parity
-        const int ex = e4m3_block_exponent(amax);
-        const Pow2 down = pow2_factors(-ex);
-        // three e4m3 terms per value; thread pairs assemble consecutive
-        // outputs: in each group of 8 outputs (4 per parity) the even thread
-        // stores groups 0, 2, .. and the odd thread groups 1, 3, ..
-        const int64_t off = pos * p.I + (int64_t)c.nb * 128;
-#pragma unroll 1
-        for (int g = 0; g < 16; ++g) {  // outputs [8 g, 8 g + 8) = acc[0..3] of each parity
-          uint32_t mine[3];
-          {
-            uint32_t a[3], b[3];
-            e4m3_terms<3>(down(acc[0]), down(acc[1]), a);
-            e4m3_terms<3>(down(acc[2]), down(acc[3]), b);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (owner && valid && par == 0) s_amax[half][j] = amax;
+        named_bar_sync(1, EPI_THREADS);
+        if (owner && lane < 16) {  // rows of both parities (lane, lane ^ 2) take part together
+          const int ex = e4m3_block_exponent(fmaxf(s_amax[0][j], s_amax[1][j]));
+          const Pow2 down = pow2_factors(-ex);
+          const int64_t off = pos * p.I + (int64_t)c.nb * 128 + 64 * half;
+          // three e4m3 terms per value; thread pairs (lane, lane ^ 2) hold the
+          // even / odd outputs and assemble 8 consecutive ones per group: the
+          // even thread stores groups 0, 2, .., the odd thread 1, 3, ..
 #pragma unroll
-            for (int t = 0; t < 3; ++t) mine[t] = a[t] | (b[t] << 16);  // 4 codes, one byte each
+          for (int g = 0; g < 8; ++g) {
+            uint32_t mine[3];
+            {
+              uint32_t a[3], b[3];
+              e4m3_terms<3>(down(acc[4 * g]), down(acc[4 * g + 1]), a);
+              e4m3_terms<3>(down(acc[4 * g + 2]), down(acc[4 * g + 3]), b);
+#pragma unroll
+              for (int t = 0; t < 3; ++t) mine[t] = a[t] | (b[t] << 16);  // 4 codes, one byte each
+            }
+#pragma unroll
+            for (int t = 0; t < 3; ++t) {
+              const uint32_t other = __shfl_xor_sync(0x0000ffffu, mine[t], 2);
+              const uint32_t ev = par ? other : mine[t], od = par ? mine[t] : other;
+              // interleave: e0 o0 e1 o1 | e2 o2 e3 o3
+              const uint32_t lo = (ev & 0xffu) | ((od & 0xffu) << 8) | ((ev & 0xff00u) << 8) | ((od & 0xff00u) << 16);
+              const uint32_t hi = ((ev >> 16) & 0xffu) | (((od >> 16) & 0xffu) << 8) |
+                                  ((ev >> 8) & 0xff0000u) | ((od & 0xff000000u));
+              uint8_t *dst = t == 0 ? p.h_t0 : (t == 1 ? p.h_t1 : p.h_t2);
+              if (valid && (g & 1) == par) *reinterpret_cast<uint2 *>(dst + off + 8 * g) = make_uint2(lo, hi);
+            }
           }
-#pragma unroll
-          for (int i = 0; i < 60; ++i) acc[i] = acc[i + 4];
-          const int o = 64 * (g >> 3) + 8 * (g & 7);
-#pragma unroll
-          for (int t = 0; t < 3; ++t) {
-            const uint32_t other = __shfl_xor_sync(0xffffffffu, mine[t], 2);
-            const uint32_t ev = par ? other : mine[t], od = par ? mine[t] : other;
-            // interleave: e0 o0 e1 o1 | e2 o2 e3 o3
-            const uint32_t lo = (ev & 0xffu) | ((od & 0xffu) << 8) | ((ev & 0xff00u) << 8) | ((od & 0xff00u) << 16);
-            const uint32_t hi = ((ev >> 16) & 0xffu) | (((od >> 16) & 0xffu) << 8) |
-                                ((ev >> 8) & 0xff0000u) | ((od & 0xff000000u));
-            uint8_t *dst = t == 0 ? p.h_t0 : (t == 1 ? p.h_t1 : p.h_t2);
-            if (valid && (g & 1) == par) *reinterpret_cast<uint2 *>(dst + off + o) = make_uint2(lo, hi);
-          }
+          if (valid && half == 0 && par == 0) p.h_scale[(int64_t)c.nb * p.Pmax + pos] = ldexpf(1.f, ex);
         }
-        if (valid && par == 0) p.h_scale[(int64_t)c.nb * p.Pmax + pos] = ldexpf(1.f, ex);
         // after the CTA's last gate/up item, publish all of them: every
         // epilogue thread makes its h stores visible to other CTAs' TMA reads
         // (proxy fence, then gpu-scope fence), the barrier orders all of
@@ -533,17 +550,13 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
             }
           }
         }
-      } else {
-        // y: value i of chunk ch is column 64 ch + 2 i + par (the row's other
-        // parity is stored by thread lane ^ 2); short code, rotating registers
+      } else if (owner && valid) {
+        // y: acc[i] is column col0 + 2 i + par, acc[32 + i] column col1 + 2 i + par
         float *dy = p.y + pos * p.H + (int64_t)c.nb * 256 + par;
-#pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-          if (valid)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dy[64 * ch + 2 * i] = acc[i];
-#pragma unroll
-          for (int i = 0; i < 96; ++i) acc[i] = acc[i + 32];
+        for (int i = 0; i < 32; ++i) {
+          dy[col0 + 2 * i] = acc[i];
+          dy[col1 + 2 * i] = acc[32 + i];
         }
       }
     }

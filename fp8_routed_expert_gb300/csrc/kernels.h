@@ -98,7 +98,7 @@ cudaError_t launch_grouped_gemm(int mode, const TmapSet &tm, const int32_t *offs
                                 uint8_t *const h_terms[3], float *h_scale, float *y, int *err,
                                 int64_t max_items, int sms, cudaStream_t s);
 // Positions per tile of the tensor-core decode FFN.
-constexpr int kDecodeTileN = 32;
+constexpr int kDecodeTileN = 16;
 // Tensor maps of the decode FFN: weights (W13 boxes of 128 rows, W2 boxes of
 // 256 rows), the token-major x terms (boxes of one row, for tile::gather4) and
 // the position-major h terms (boxes of kDecodeTileN rows).

@@ -14,7 +14,7 @@ using namespace fp8moe;
 
 namespace {
 
-constexpr int64_t kGemvMaxT = 64;  // MOE_PATH_AUTO: GEMV path up to this T
+constexpr int64_t kDecodeMaxT = 64;  // MOE_PATH_AUTO: tensor-core decode path up to this T
 
 struct TimingRec {
   cudaEvent_t a, b;
@@ -133,7 +133,7 @@ void drain_timing(moe_ctx *c) {
 
 // The path a forward of T tokens takes.
 int resolve_path(const moe_ctx *c, int64_t T) {
-  int path = c->path != MOE_PATH_AUTO ? c->path : (T <= kGemvMaxT ? MOE_PATH_GEMV : MOE_PATH_GEMM);
+  int path = c->path != MOE_PATH_AUTO ? c->path : (T <= kDecodeMaxT ? MOE_PATH_TCGEMV : MOE_PATH_GEMM);
   // the tensor-core paths' down items are 256 output rows wide
   if ((path == MOE_PATH_GEMM || path == MOE_PATH_TCGEMV) && c->cfg.hidden % 256 != 0) path = MOE_PATH_GEMV;
   return path;

@@ -143,14 +143,15 @@ void moe_free(moe_ctx *ctx);
 const char *moe_strerror(int code);
 
 /*
- * Path selection.  MOE_PATH_AUTO picks the grouped-GEMV path for
- * T <= 64 and the tensor-core grouped-GEMM path above; the other values force
- * one path (all compute the same layer).
+ * Path selection.  MOE_PATH_AUTO picks the tensor-core decode path for
+ * T <= 64 and the tensor-core grouped-GEMM path above (both need H % 256 == 0;
+ * otherwise the grouped-GEMV path runs); the other values force one path (all
+ * compute the same layer).
  *   MOE_PATH_GEMV   e4m3 weights dequantised in registers, mma.sync f16
  *                   (activations as f16 hi/lo pairs);
  *   MOE_PATH_GEMM   tcgen05 grouped GEMM, tiles of 128 positions;
- *   MOE_PATH_TCGEMV tcgen05 grouped GEMV, tiles of 16 positions (the weight
- *                   rows are the MMA's M operand, the expert's tokens its N).
+ *   MOE_PATH_TCGEMV tcgen05 decode FFN: gate/up and down in one launch, tiles
+ *                   of 16 positions (the weight rows are the MMA's N operand).
  */
 #define MOE_PATH_AUTO 0
 #define MOE_PATH_GEMV 1

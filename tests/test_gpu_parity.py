@@ -304,11 +304,12 @@ def test_kernel_timing_api():
     n0 = layer.launch_count()
     for _ in range(3):
         run(layer, x, dw, fam.top_k)
-    assert layer.launch_count() - n0 == 3 * 4   # fused routing, gate/up, down, combine
-    for name in ("route", "gate_up", "down", "combine"):
+    assert layer.resolved_path(8) == "tcgemv"
+    assert layer.launch_count() - n0 == 3 * 3   # routing, fused gate/up + down, combine
+    for name in ("route", "gate_up", "combine"):
         ms, n = layer.kernel_time(name)
         assert n == 3 and ms > 0, name
     layer.set_timing(["gate_up"])
     run(layer, x, dw, fam.top_k)
-    assert layer.kernel_time("gate_up")[1] == 1 and layer.kernel_time("down")[1] == 0
+    assert layer.kernel_time("gate_up")[1] == 1 and layer.kernel_time("route")[1] == 0
     layer.set_timing(())
