@@ -124,15 +124,14 @@ cudaError_t launch_decode_ffn(const DecodeMaps &maps, const int32_t *offsets,
 cudaError_t launch_act_quant_tokens(const __nv_bfloat16 *x, int64_t T, int64_t H, uint8_t *a_hi,
                                     uint8_t *a_lo, float *a_scale, int64_t a_ld, int sms,
                                     cudaStream_t s);
-// T <= 64 on the tensor-core decode path: logits, per-token activation terms,
-// selection and the pair sort in one launch.  tickets: kSmallTicketInts ints,
-// zero between calls; counters [n_counters] are cleared.
-constexpr int kSmallTicketInts = 16;
+// T <= 64 on the tensor-core decode path: logits and per-token activation
+// terms, then (one CTA, chained by programmatic dependent launch) selection
+// and the pair sort; counters [n_counters] are cleared.
 float route_small_gamma(int64_t H, int64_t E);
 cudaError_t launch_route_small(const __nv_bfloat16 *x, int64_t T, const float *W, const float *bias,
                                int64_t E, int64_t H, int k, float *logits, float *wnorm, float *xss,
                                uint8_t *a_hi, uint8_t *a_lo, float *a_scale, int64_t a_ld,
-                               int32_t *tickets, int32_t *counters, int n_counters, int32_t *idx,
+                               int32_t *counters, int n_counters, int32_t *idx,
                                float *wts, int32_t *counts, int32_t *offsets, int32_t *perm,
                                int32_t *inv, int32_t *active, int32_t *n_active,
                                int32_t *tile_offsets, int tile_m, int *err, cudaStream_t s);

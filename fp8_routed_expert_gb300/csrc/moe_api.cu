@@ -44,7 +44,6 @@ struct moe_ctx {
   TmapSet tm_gemm1, tm_gemm2;                    // activation terms (workspace) + last weights
   DecodeMaps dmaps;                              // tensor-core decode FFN operands
   float *xss = nullptr;                          // per-(token, 128 columns) sums of squares of x
-  int32_t *tickets = nullptr;                    // small-batch routing tickets (0 between calls)
   int32_t *done13 = nullptr;                     // decode FFN per-tile counters
   const void *tm_w13_ptr = nullptr, *tm_w2_ptr = nullptr;  // weights the maps in .b describe
   const void *dmaps_w13 = nullptr, *dmaps_w2 = nullptr;    // weights dmaps describe
@@ -151,7 +150,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
     if (T <= kRouterWarpMaxT) {
       Timed tm(c, MOE_K_ROUTE, s);
       CUDA_TRY(launch_route_small(x, T, rw, rb, E, H, k, c->logits, c->wnorm, c->xss, c->a_hi,
-                                  c->a_lo, c->a_scale, Pm, c->tickets, c->done13, (int)max_tiles,
+                                  c->a_lo, c->a_scale, Pm, c->done13, (int)max_tiles,
                                   c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv, c->active,
                                   c->n_active, c->tile_offsets, kDecodeTileN, c->err, s));
     } else {
@@ -358,7 +357,6 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->active, (size_t)E * 4},
       {(void **)&c->n_active, 16},
       {(void **)&c->ticket, 16},
-      {(void **)&c->tickets, (size_t)kSmallTicketInts * 4},
       {(void **)&c->done13, (size_t)((Pm + kDecodeTileN - 1) / kDecodeTileN + E + 1) * 4},
       {(void **)&c->xss, (size_t)(Tm * (H / 128)) * 4},
       {(void **)&c->xnorm, (size_t)Tm * 4},

@@ -11,7 +11,7 @@ struct SortOut {
 };
 
 // Shared memory (bytes) of cta_counting_sort with NW warps and E experts.
-inline size_t cta_sort_smem(int NW, int E) { return (size_t)((NW + 1) * E + 1 + 64) * sizeof(int); }
+__host__ __device__ inline size_t cta_sort_smem(int NW, int E) { return (size_t)((NW + 1) * E + 1 + 64) * sizeof(int); }
 
 // Exclusive scan of one int per thread over the CTA; *total gets the sum.
 // Every thread of the CTA must call it.  tmp: >= 33 ints of shared memory.

@@ -447,20 +447,27 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_decode_kernel(
   if (threadIdx.x == 0) *ticket = 0;
 }
 
-// ------------------------------------------------------------------ small-batch routing, tiled
-// One launch for T <= 64 (the tensor-core decode path).  The grid is
-// (expert blocks) x (token blocks of 8).  CTA (eb, tb) computes the logits of
-// EPC experts for the tb's tokens: WPE = 8 / EPC warps share one expert's row,
-// each over a contiguous range of 128-column chunks; a lane keeps four
-// partial sums (one per column of its 4-column slice), so the longest rounding
-// chain is nch_w + 2 (lane) + 5 (butterfly) + log2(WPE) (pairwise over warps)
-// + 1 (bias), nch_w = ceil(H / 128 / WPE).  The same CTAs split every token
-// row of the block into per-(token, 128-column chunk) units: two e4m3 terms
-// with one power-of-two scale (the tensor-core GEMV's activation operand,
-// token-major) and the chunk's sum of squares (for ||x_t||).
-// The last CTA of a token block (ticket per block) selects the top k of its
-// tokens, one warp per token; the last selecting CTA (second ticket) sorts
-// the pairs by expert and clears the work counters of the expert kernels.
+// ------------------------------------------------------------------ small-batch routing
+// T <= 64 on the tensor-core decode path, in two launches chained by
+// programmatic dependent launch.
+//
+// Logits: the grid is (expert blocks) x (token blocks of 8).  CTA (eb, tb)
+// computes the logits of EPC experts for the tb's tokens: WPE = 8 / EPC warps
+// share one expert's row, each over a contiguous range of 128-column chunks
+// (four chunks' loads in flight at a time); a lane keeps four partial sums
+// (one per column of its 4-column slice), so the longest rounding chain is
+// nch_w + 2 (lane) + 5 (butterfly) + log2(WPE) (pairwise over warps) + 1
+// (bias), nch_w = ceil(H / 128 / WPE).  The same CTAs split every token row of
+// the block into per-(token, 128-column chunk) units: two e4m3 terms with one
+// power-of-two scale (the tensor-core FFN's activation operand, token-major)
+// and the chunk's sum of squares (for ||x_t||).
+//
+// Selection and sort: one CTA.  Each warp takes tokens t = warp, warp + NW,
+// ..: it holds the token's logits and bounds in registers (EPL per lane),
+// selects the top k and certifies the order as the general selection does;
+// a token the bound cannot certify goes through the exact path
+// (select_token).  The CTA then sorts the pairs by expert from shared memory
+// and clears the FFN's work counters.
 constexpr int kSmallTB = 8;  // tokens per token block
 
 struct RouteSmallArgs {
@@ -471,27 +478,24 @@ struct RouteSmallArgs {
   uint8_t *a_hi, *a_lo;       // [T, H] activation terms (token-major)
   float *a_scale;             // [H/128][a_ld] power-of-two scales
   int64_t a_ld;
-  int32_t *tickets;           // [kSmallTB + 1], 0 between calls
   int32_t *counters;          // [n_counters] cleared for the expert kernels
   int n_counters;
   int tile_m;
   SortOut so;
 };
 
-__global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(RouteSmallArgs r) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+__global__ void __launch_bounds__(32 * kRouteWarps) route_logits_small_kernel(RouteSmallArgs r) {
   __shared__ float part_l[kRouteWarps][kSmallTB];
   __shared__ float part_w[kRouteWarps];
-  __shared__ int s_last;
   const SelectArgs &a = r.sel;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int64_t E = a.E, H = a.H, T = a.T;
   const int64_t nch = H / 128;
   const int epc = r.epc, wpe = kRouteWarps / epc;
-  const int eb = blockIdx.x, tb = blockIdx.y, n_eb = gridDim.x, n_tb = gridDim.y;
+  const int eb = blockIdx.x, tb = blockIdx.y, n_eb = gridDim.x;
   const int64_t t0 = (int64_t)tb * kSmallTB;
   const int nt = (int)((T - t0) < kSmallTB ? (T - t0) : kSmallTB);
-  pdl_trigger();
+  pdl_trigger();  // the selection kernel may be scheduled; it waits for this grid
 
   // ---- logits of EPC experts for the block's tokens
   const int eslot = wid / wpe, part = wid % wpe;
@@ -504,21 +508,32 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(RouteSmal
     for (int i = 0; i < 4; ++i) acc[j][i] = 0.f;
   if (e < E) {
     const float *w = a.W + e * H;
-    for (int64_t c = c_lo; c < c_hi; ++c) {
-      const int64_t h = c * 128 + 4 * lane;
-      const float4 wv = __ldg(reinterpret_cast<const float4 *>(w + h));
-      wss[0] = fmaf(wv.x, wv.x, wss[0]);
-      wss[1] = fmaf(wv.y, wv.y, wss[1]);
-      wss[2] = fmaf(wv.z, wv.z, wss[2]);
-      wss[3] = fmaf(wv.w, wv.w, wss[3]);
+    for (int64_t c0 = c_lo; c0 < c_hi; c0 += 4) {
+      // four chunks' loads in flight, then their products
+      float4 wv[4];
+      uint2 xv[4][kSmallTB];
 #pragma unroll
-      for (int j = 0; j < kSmallTB; ++j) {
-        if (j < nt) {
-          const uint2 xv = __ldg(reinterpret_cast<const uint2 *>(a.x + (t0 + j) * H + h));
-          acc[j][0] = fmaf(bf16_bits_to_float(xv.x & 0xffffu), wv.x, acc[j][0]);
-          acc[j][1] = fmaf(bf16_bits_to_float(xv.x >> 16), wv.y, acc[j][1]);
-          acc[j][2] = fmaf(bf16_bits_to_float(xv.y & 0xffffu), wv.z, acc[j][2]);
-          acc[j][3] = fmaf(bf16_bits_to_float(xv.y >> 16), wv.w, acc[j][3]);
+      for (int u = 0; u < 4; ++u) {
+        const int64_t h = (c0 + u) * 128 + 4 * lane;
+        const bool in = c0 + u < c_hi;
+        wv[u] = in ? __ldg(reinterpret_cast<const float4 *>(w + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < kSmallTB; ++j)
+          xv[u][j] = (in && j < nt) ? __ldg(reinterpret_cast<const uint2 *>(a.x + (t0 + j) * H + h))
+                                    : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        wss[0] = fmaf(wv[u].x, wv[u].x, wss[0]);
+        wss[1] = fmaf(wv[u].y, wv[u].y, wss[1]);
+        wss[2] = fmaf(wv[u].z, wv[u].z, wss[2]);
+        wss[3] = fmaf(wv[u].w, wv[u].w, wss[3]);
+#pragma unroll
+        for (int j = 0; j < kSmallTB; ++j) {
+          acc[j][0] = fmaf(bf16_bits_to_float(xv[u][j].x & 0xffffu), wv[u].x, acc[j][0]);
+          acc[j][1] = fmaf(bf16_bits_to_float(xv[u][j].x >> 16), wv[u].y, acc[j][1]);
+          acc[j][2] = fmaf(bf16_bits_to_float(xv[u][j].y & 0xffffu), wv[u].z, acc[j][2]);
+          acc[j][3] = fmaf(bf16_bits_to_float(xv[u][j].y >> 16), wv[u].w, acc[j][3]);
         }
       }
     }
@@ -570,42 +585,131 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_small_kernel(RouteSmal
       for (int q = 0; q + w < wpe; q += 2 * w) v[q] = v[q] + v[q + w];
     if (ee < E && j < nt) r.logits_w[(t0 + j) * E + ee] = v[0];
     if (ee < E && j == 0 && tb == 0) {
-      float s = 0.f;
-      for (int q = 0; q < wpe; ++q) s += part_w[es * wpe + q];
-      r.wnorm_w[ee] = sqrtf(s);
+      float ssum = 0.f;
+      for (int q = 0; q < wpe; ++q) ssum += part_w[es * wpe + q];
+      r.wnorm_w[ee] = sqrtf(ssum);
     }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(&r.tickets[tb], 1) == n_eb - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+}
 
-  // ---- selection: one warp per token of the block
+// Top k of token t from register-held logits (EPL per lane, expert
+// lane + 32 i); the same selection, certification and weights as
+// select_token's certified case.  Returns false (writing nothing) when the
+// bound cannot certify the order or a logit is not finite; the caller then
+// runs the exact path.
+template <int EPL>
+__device__ bool select_fast(const SelectArgs &a, int64_t t, float xn, int32_t *idx_s) {
+  const int lane = threadIdx.x & 31;
+  const int E = (int)a.E, k = a.k;
+  const float tiny = (float)a.H * 1.0e-37f;
+  float v[EPL], b[EPL];
+  bool finite = true;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      float lv = __ldcg(a.logits + t * a.E + e);
+      float bb = a.gamma * xn * __ldcg(a.wnorm + e) * 1.01f + tiny;
+      if (a.bias != nullptr) {
+        const float bi = __ldg(a.bias + e);
+        lv += bi;
+        bb += fabsf(bi) * 1.2e-7f;
+      }
+      finite = finite && isfinite(lv);
+      v[i] = lv;
+      b[i] = bb;
+    } else {
+      v[i] = -INFINITY;
+      b[i] = 0.f;
+    }
+  }
+  if (!__all_sync(0xffffffffu, finite)) return false;
+  uint32_t taken = 0;
+  int sel_e = -1;
+  float sel_v = 0.f, sel_b = 0.f;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY, bb = 0.f;
+    int be = INT_MAX;
+#pragma unroll
+    for (int i = 0; i < EPL; ++i) {
+      const int e = lane + 32 * i;
+      if (!((taken >> i) & 1u) && e < E && (be == INT_MAX || v[i] > bv)) {
+        bv = v[i];
+        be = e;
+        bb = b[i];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      const float ob = __shfl_xor_sync(0xffffffffu, bb, o);
+      if (oe != INT_MAX && (be == INT_MAX || ov > bv || (ov == bv && oe < be))) {
+        bv = ov;
+        be = oe;
+        bb = ob;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == r) {
+      sel_e = be;
+      sel_v = bv;
+      sel_b = bb;
+    }
+  }
+  // certify: every selected lower bound above every other upper bound, and
+  // adjacent selected experts separated by their bounds
+  float upper_rest = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < EPL; ++i)
+    if (!((taken >> i) & 1u) && lane + 32 * i < E) upper_rest = fmaxf(upper_rest, v[i] + b[i]);
+  upper_rest = warp_max(upper_rest);
+  const float lo_sel = (lane < k) ? sel_v - sel_b : INFINITY;
+  const float hi_next = __shfl_down_sync(0xffffffffu, (lane < k) ? sel_v + sel_b : -INFINITY, 1);
+  const bool ordered = (lane + 1 >= k) || (lo_sel > hi_next);
+  const float min_lo = -warp_max(-lo_sel);
+  const bool certified = __all_sync(0xffffffffu, ordered) && (k == E || min_lo > upper_rest) &&
+                         isfinite(min_lo);
+  if (!certified) return false;
+  const float l0 = __shfl_sync(0xffffffffu, sel_v, 0);
+  const float ex = (lane < k) ? __expf(sel_v - l0) : 0.f;
+  const float z = warp_sum(ex);
+  if (lane < k) {
+    a.idx[t * k + lane] = sel_e;
+    a.wts[t * k + lane] = ex / z;
+    idx_s[t * k + lane] = sel_e;
+  }
+  return true;
+}
+
+template <int EPL, int NW>
+__global__ void __launch_bounds__(32 * NW, 1) route_select_small_kernel(RouteSmallArgs r) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const SelectArgs &a = r.sel;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t E = a.E, T = a.T, nch = a.H / 128;
+  const int k = a.k;
+  // shared memory: [NW] exact-path scratch (E doubles + 2E floats), the sort's
+  // scratch, the selected experts [T k]
   double *lg64 = reinterpret_cast<double *>(smem_raw) + (size_t)wid * E;
-  float *lg = reinterpret_cast<float *>(smem_raw + (size_t)kRouteWarps * E * sizeof(double)) + (size_t)wid * 2 * E;
-  if (wid < nt) {
-    const int64_t t = t0 + wid;
+  float *lg = reinterpret_cast<float *>(smem_raw + (size_t)NW * E * sizeof(double)) + (size_t)wid * 2 * E;
+  int *sort_smem = reinterpret_cast<int *>(smem_raw + (size_t)NW * E * (sizeof(double) + 2 * sizeof(float)));
+  int32_t *idx_s = sort_smem + cta_sort_smem(NW, (int)E) / sizeof(int);
+  pdl_wait();  // logits, norms and activation units come from the previous kernel
+  pdl_trigger();
+  for (int64_t t = wid; t < T; t += NW) {
     float ss = 0.f;
     for (int64_t c = lane; c < nch; c += 32) ss += __ldcg(r.xss + t * nch + c);
     const float xn = sqrtf(warp_sum(ss));
-    select_token(a, t, xn, lg, lg + E, lg64);
+    if (!select_fast<EPL>(a, t, xn, idx_s)) {
+      select_token(a, t, xn, lg, lg + E, lg64);
+      __syncwarp();
+      if (lane < k) idx_s[t * k + lane] = a.idx[t * k + lane];
+    }
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    r.tickets[tb] = 0;
-    s_last = atomicAdd(&r.tickets[kSmallTB], 1) == n_tb - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
-  // ---- stable sort of the pairs by expert; clear the expert kernels' counters
   for (int i = threadIdx.x; i < r.n_counters; i += blockDim.x) r.counters[i] = 0;
-  cta_counting_sort<kRouteWarps>(a.idx, T * a.k, (int)E, r.tile_m, r.so, reinterpret_cast<int *>(smem_raw), a.err);
-  if (threadIdx.x == 0) r.tickets[kSmallTB] = 0;
+  __syncthreads();
+  cta_counting_sort<NW>(idx_s, T * k, (int)E, r.tile_m, r.so, sort_smem, a.err);
 }
 
 // f16 copies of every token (the GEMV path above the fused-routing size).
@@ -819,10 +923,23 @@ float route_small_gamma(int64_t H, int64_t E) {
   return nextafterf((float)(g * (1.0 + 1e-6)), INFINITY);
 }
 
+namespace {
+template <int EPL, int NW>
+cudaError_t launch_select_small(const RouteSmallArgs &r, cudaStream_t s) {
+  const int64_t E = r.sel.E;
+  const size_t smem = (size_t)NW * E * (sizeof(double) + 2 * sizeof(float)) + cta_sort_smem(NW, (int)E) +
+                      (size_t)r.sel.T * r.sel.k * sizeof(int32_t);
+  auto kern = route_select_small_kernel<EPL, NW>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(kern, dim3(1), dim3(32 * NW), smem, s, r);
+}
+}  // namespace
+
 cudaError_t launch_route_small(const __nv_bfloat16 *x, int64_t T, const float *W, const float *bias,
                                int64_t E, int64_t H, int k, float *logits, float *wnorm, float *xss,
                                uint8_t *a_hi, uint8_t *a_lo, float *a_scale, int64_t a_ld,
-                               int32_t *tickets, int32_t *counters, int n_counters, int32_t *idx,
+                               int32_t *counters, int n_counters, int32_t *idx,
                                float *wts, int32_t *counts, int32_t *offsets, int32_t *perm,
                                int32_t *inv, int32_t *active, int32_t *n_active,
                                int32_t *tile_offsets, int tile_m, int *err, cudaStream_t s) {
@@ -836,17 +953,20 @@ cudaError_t launch_route_small(const __nv_bfloat16 *x, int64_t T, const float *W
   r.a_lo = a_lo;
   r.a_scale = a_scale;
   r.a_ld = a_ld;
-  r.tickets = tickets;
   r.counters = counters;
   r.n_counters = n_counters;
   r.tile_m = tile_m;
   r.so = SortOut{counts, offsets, perm, inv, active, n_active, tile_offsets};
-  const size_t smem = route_decode_smem(E);
-  cudaError_t e = cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   dim3 grid((unsigned)((E + r.epc - 1) / r.epc), (unsigned)((T + kSmallTB - 1) / kSmallTB));
-  route_small_kernel<<<grid, 32 * kRouteWarps, smem, s>>>(r);
-  return cudaGetLastError();
+  route_logits_small_kernel<<<grid, 32 * kRouteWarps, 0, s>>>(r);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (E <= 32) return launch_select_small<1, 16>(r, s);
+  if (E <= 64) return launch_select_small<2, 16>(r, s);
+  if (E <= 128) return launch_select_small<4, 16>(r, s);
+  if (E <= 256) return launch_select_small<8, 16>(r, s);
+  if (E <= 512) return launch_select_small<16, 16>(r, s);
+  return launch_select_small<32, 8>(r, s);
 }
 
 cudaError_t launch_router_logits_tiled(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
