@@ -408,8 +408,8 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv2_kernel(
 // out[t, :] = bf16_rne( sum_{r=0}^{k-1} w[t, r] * y[inv[t k + r], :] ), summed
 // in router rank order with one fma chain per element (WARP BACKENDS.md,
 // "Coherent memory": partials reduced in original router order) and no atomics.
-__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y,
-                                                      const int32_t *__restrict__ inv,
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, int n_planes,
+                                                      int64_t plane, const int32_t *__restrict__ inv,
                                                       const float *__restrict__ wts, int64_t T,
                                                       int k, int64_t H,
                                                       __nv_bfloat16 *__restrict__ out) {
@@ -422,7 +422,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
     for (int r = 0; r < k; ++r) {
       const int64_t pos = inv[t * k + r];
       const float w = wts[t * k + r];
-      const float4 v = __ldg(reinterpret_cast<const float4 *>(y + pos * H + j));
+      const float *yp = y + pos * H + j;
+      float4 v = __ldg(reinterpret_cast<const float4 *>(yp));
+      for (int q = 1; q < n_planes; ++q) {
+        const float4 u = __ldg(reinterpret_cast<const float4 *>(yp + q * plane));
+        v.x += u.x;
+        v.y += u.y;
+        v.z += u.z;
+        v.w += u.w;
+      }
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
@@ -510,10 +518,11 @@ cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, con
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine(const float *y, const int32_t *inv, const float *wts, int64_t T, int k,
-                           int64_t H, __nv_bfloat16 *out, cudaStream_t s) {
+cudaError_t launch_combine(const float *y, int n_planes, int64_t plane, const int32_t *inv,
+                           const float *wts, int64_t T, int k, int64_t H, __nv_bfloat16 *out,
+                           cudaStream_t s) {
   return launch_pdl(combine_kernel, dim3((unsigned)T, (unsigned)((H + 1023) / 1024)), dim3(256), 0, s, y,
-                    inv, wts, T, k, H, out);
+                    n_planes, plane, inv, wts, T, k, H, out);
 }
 
 }  // namespace fp8moe

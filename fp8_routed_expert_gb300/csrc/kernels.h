@@ -111,14 +111,16 @@ struct DecodeMaps {
 // (tile_offsets counted in tiles of kDecodeTileN positions).  x terms are
 // token-major with scales x_scale[H/128][x_ld]; h is written as three e4m3
 // terms with one power-of-two scale per (position, 128 outputs), h_scale
-// [I/128][Pmax]; y f32 [Pmax, H].  done13 [max_tiles] must be zero on entry.
+// [I/128][Pmax]; y f32 in three term planes [3][y_plane] of [P, H] (y of a
+// pair is the sum of its three rows).  done13 [max_tiles + 1] (per-tile
+// counters, then the work-queue head) must be zero on entry.
 // Needs H % 256 == 0.
 cudaError_t launch_decode_ffn(const DecodeMaps &maps, const int32_t *offsets,
                               const int32_t *tile_offsets, const int32_t *perm, int k,
                               const float *x_scale, int64_t x_ld, const float *s13, const float *s2,
                               int E, int64_t H, int64_t I, int64_t Pmax, uint8_t *const h_terms[3],
-                              float *h_scale, float *y, int32_t *done13, int *err, int64_t max_tiles,
-                              int sms, cudaStream_t s);
+                              float *h_scale, float *y, int64_t y_plane, int32_t *done13, int *err,
+                              int64_t max_tiles, int sms, cudaStream_t s);
 // Per-token activation terms (two e4m3 terms, one power-of-two scale per
 // (token, 128 columns)); the token-major operand of the decode FFN.
 cudaError_t launch_act_quant_tokens(const __nv_bfloat16 *x, int64_t T, int64_t H, uint8_t *a_hi,
@@ -135,7 +137,10 @@ cudaError_t launch_route_small(const __nv_bfloat16 *x, int64_t T, const float *W
                                float *wts, int32_t *counts, int32_t *offsets, int32_t *perm,
                                int32_t *inv, int32_t *active, int32_t *n_active,
                                int32_t *tile_offsets, int tile_m, int *err, cudaStream_t s);
-cudaError_t launch_combine(const float *y, const int32_t *inv, const float *wts, int64_t T, int k,
-                           int64_t H, __nv_bfloat16 *out, cudaStream_t s);
+// out[t] = sum_r wts[t, r] y[inv[t, r]], y of a pair being the sum of its rows
+// in n_planes planes (stride plane) added in plane order.
+cudaError_t launch_combine(const float *y, int n_planes, int64_t plane, const int32_t *inv,
+                           const float *wts, int64_t T, int k, int64_t H, __nv_bfloat16 *out,
+                           cudaStream_t s);
 
 }  // namespace fp8moe

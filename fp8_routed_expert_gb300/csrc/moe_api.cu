@@ -150,7 +150,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
     if (T <= kRouterWarpMaxT) {
       Timed tm(c, MOE_K_ROUTE, s);
       CUDA_TRY(launch_route_small(x, T, rw, rb, E, H, k, c->logits, c->wnorm, c->xss, c->a_hi,
-                                  c->a_lo, c->a_scale, Pm, c->done13, (int)max_tiles,
+                                  c->a_lo, c->a_scale, Pm, c->done13, (int)max_tiles + 1,
                                   c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv, c->active,
                                   c->n_active, c->tile_offsets, kDecodeTileN, c->err, s));
     } else {
@@ -168,7 +168,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
         Timed tm(c, MOE_K_PERMUTE, s);
         CUDA_TRY(launch_permute(c->idx, P, (int)E, kDecodeTileN, c->counts, c->offsets, c->perm,
                                 c->inv, c->active, c->n_active, c->tile_offsets, nullptr, c->done13,
-                                (int)max_tiles, c->err, s));
+                                (int)max_tiles + 1, c->err, s));
       }
       {
         Timed tm(c, MOE_K_ACT_QUANT, s);
@@ -186,12 +186,12 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
     {
       Timed tm(c, MOE_K_GATE_UP, s);
       CUDA_TRY(launch_decode_ffn(c->dmaps, c->offsets, c->tile_offsets, c->perm, k, c->a_scale, Pm,
-                                 s13, s2, (int)E, H, I, Pm, c->h_t, c->h_scale, c->y, c->done13,
-                                 c->err, max_tiles, c->sms, s));
+                                 s13, s2, (int)E, H, I, Pm, c->h_t, c->h_scale, c->y, P * H,
+                                 c->done13, c->err, max_tiles, c->sms, s));
     }
     {
       Timed tm(c, MOE_K_COMBINE, s);
-      CUDA_TRY(launch_combine(c->y, c->inv, c->wts, T, k, H, out, s));
+      CUDA_TRY(launch_combine(c->y, 3, P * H, c->inv, c->wts, T, k, H, out, s));
     }
     c->last_T = T;
     c->last_k = k;
@@ -268,7 +268,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
   }
   {
     Timed tm(c, MOE_K_COMBINE, s);
-    CUDA_TRY(launch_combine(c->y, c->inv, c->wts, T, k, H, out, s));
+    CUDA_TRY(launch_combine(c->y, 1, 0, c->inv, c->wts, T, k, H, out, s));
   }
   c->last_T = T;
   c->last_k = k;
@@ -365,7 +365,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->x16, (size_t)(Tm * H) * 2},
       {(void **)&c->xscale, (size_t)Tm * 4},
       {(void **)&c->h, (size_t)(Pm * I) * 4},
-      {(void **)&c->y, (size_t)(Pm * H) * 4},
+      {(void **)&c->y, (size_t)(3 * Pm * H) * 4},  // three term planes on the decode path
       {(void **)&c->xin, (size_t)(Tm * H) * 2},
       {(void **)&c->xout, (size_t)(Tm * H) * 2},
       {(void **)&c->err, 16},
@@ -534,6 +534,7 @@ int moe_debug_copy(moe_ctx *c, const char *name, void *dst, int64_t capacity, in
   if (!strcmp(name, "logits")) { p = c->logits; n = T * E * 4; }
   else if (!strcmp(name, "h")) { p = c->h; n = P * I * 4; }
   else if (!strcmp(name, "y")) { p = c->y; n = P * H * 4; }
+  else if (!strcmp(name, "y_terms")) { p = c->y; n = 3 * P * H * 4; }
   else if (!strcmp(name, "x16")) { p = c->x16; n = T * H * 2; }
   else return MOE_ERR_ARG;
   if (nbytes) *nbytes = n;

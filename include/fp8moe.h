@@ -187,7 +187,9 @@ const char *moe_kernel_name(int kernel);
 /*
  * moe_debug_copy - copy a workspace buffer of the last forward into a caller
  * device buffer, for tests: "logits" f32 [T,E], "h" f32 [P,I] (GEMV path,
- * position order), "y" f32 [P,H] (position order), "x16" f16 [T,H].  Copies
+ * position order), "y" f32 [P,H] (position order; GEMV and GEMM paths),
+ * "y_terms" f32 [3,P,H] (tensor-core decode path: y of a position is the sum
+ * of its three rows, one per h term), "x16" f16 [T,H].  Copies
  * min(capacity, size) bytes on `stream` and stores the buffer's full size in
  * *nbytes (may be NULL).
  */

@@ -127,7 +127,11 @@ def test_tensor_core_paths_y_match_oracle(T, path):
     check_routing(r, ref, fam.n_experts)
     check_output(out, ref)
     P = T * k
-    y = layer.debug_buffer("y", torch.float32, (P, fam.hidden)).cpu().numpy().astype(np.float64)
+    if path == "tcgemv":  # one plane per h term; y of a position is their sum
+        y3 = layer.debug_buffer("y_terms", torch.float32, (3, P, fam.hidden)).cpu().numpy()
+        y = y3.astype(np.float64).sum(axis=0)
+    else:
+        y = layer.debug_buffer("y", torch.float32, (P, fam.hidden)).cpu().numpy().astype(np.float64)
     ref_y = ref["y"].reshape(P, fam.hidden)[ref["perm"]]
     rel = np.linalg.norm(y - ref_y) / np.linalg.norm(ref_y)
     assert rel < 2e-4, rel
