@@ -408,41 +408,59 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv2_kernel(
 // out[t, :] = bf16_rne( sum_{r=0}^{k-1} w[t, r] * y[inv[t k + r], :] ), summed
 // in router rank order with one fma chain per element (WARP BACKENDS.md,
 // "Coherent memory": partials reduced in original router order) and no atomics.
-__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ y, int n_planes,
-                                                      int64_t plane, const int32_t *__restrict__ inv,
-                                                      const float *__restrict__ wts, int64_t T,
-                                                      int k, int64_t H,
-                                                      __nv_bfloat16 *__restrict__ out) {
-  pdl_wait();
+// y of a pair is the sum of its rows in NP planes, added in plane order.
+// Thread: one 4-column group of one token; the loads of up to kCombineBatch
+// pairs (all planes) are issued before any is used.
+constexpr int kCombineThreads = 64;
+constexpr int kCombineBatch = 8;
+
+template <int NP>
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float *__restrict__ y, int64_t plane,
+                                                                  const int32_t *__restrict__ inv,
+                                                                  const float *__restrict__ wts, int64_t T,
+                                                                  int k, int64_t H,
+                                                                  __nv_bfloat16 *__restrict__ out) {
   const int64_t t = blockIdx.x;
-  if (t >= T) return;
-  for (int64_t j = 4 * (int64_t)(blockIdx.y * blockDim.x + threadIdx.x); j < H;
-       j += 4 * (int64_t)blockDim.x * gridDim.y) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = 0; r < k; ++r) {
-      const int64_t pos = inv[t * k + r];
-      const float w = wts[t * k + r];
-      const float *yp = y + pos * H + j;
-      float4 v = __ldg(reinterpret_cast<const float4 *>(yp));
-      for (int q = 1; q < n_planes; ++q) {
-        const float4 u = __ldg(reinterpret_cast<const float4 *>(yp + q * plane));
-        v.x += u.x;
-        v.y += u.y;
-        v.z += u.z;
-        v.w += u.w;
+  const int64_t j = 4 * ((int64_t)blockIdx.y * kCombineThreads + threadIdx.x);
+  pdl_wait();
+  if (t >= T || j >= H) return;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r0 = 0; r0 < k; r0 += kCombineBatch) {
+    float4 v[kCombineBatch][NP];
+    float w[kCombineBatch];
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      if (r0 + u < k) {
+        const int64_t pos = __ldg(inv + t * k + r0 + u);
+        w[u] = __ldg(wts + t * k + r0 + u);
+#pragma unroll
+        for (int q = 0; q < NP; ++q) v[u][q] = __ldg(reinterpret_cast<const float4 *>(y + q * plane + pos * H + j));
       }
-      acc.x = fmaf(w, v.x, acc.x);
-      acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z);
-      acc.w = fmaf(w, v.w, acc.w);
     }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-    uint2 o;
-    o.x = *reinterpret_cast<uint32_t *>(&lo);
-    o.y = *reinterpret_cast<uint32_t *>(&hi);
-    *reinterpret_cast<uint2 *>(out + t * H + j) = o;
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      if (r0 + u < k) {
+        float4 s4 = v[u][0];
+#pragma unroll
+        for (int q = 1; q < NP; ++q) {
+          s4.x += v[u][q].x;
+          s4.y += v[u][q].y;
+          s4.z += v[u][q].z;
+          s4.w += v[u][q].w;
+        }
+        acc.x = fmaf(w[u], s4.x, acc.x);
+        acc.y = fmaf(w[u], s4.y, acc.y);
+        acc.z = fmaf(w[u], s4.z, acc.z);
+        acc.w = fmaf(w[u], s4.w, acc.w);
+      }
+    }
   }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 o;
+  o.x = *reinterpret_cast<uint32_t *>(&lo);
+  o.y = *reinterpret_cast<uint32_t *>(&hi);
+  *reinterpret_cast<uint2 *>(out + t * H + j) = o;
 }
 
 // ---------------------------------------------------------------- launchers
@@ -521,8 +539,11 @@ cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, con
 cudaError_t launch_combine(const float *y, int n_planes, int64_t plane, const int32_t *inv,
                            const float *wts, int64_t T, int k, int64_t H, __nv_bfloat16 *out,
                            cudaStream_t s) {
-  return launch_pdl(combine_kernel, dim3((unsigned)T, (unsigned)((H + 1023) / 1024)), dim3(256), 0, s, y,
-                    n_planes, plane, inv, wts, T, k, H, out);
+  const dim3 grid((unsigned)T, (unsigned)((H / 4 + kCombineThreads - 1) / kCombineThreads));
+  if (n_planes == 3)
+    return launch_pdl(combine_kernel<3>, grid, dim3(kCombineThreads), 0, s, y, plane, inv, wts, T, k, H, out);
+  if (n_planes != 1) return cudaErrorInvalidValue;
+  return launch_pdl(combine_kernel<1>, grid, dim3(kCombineThreads), 0, s, y, plane, inv, wts, T, k, H, out);
 }
 
 }  // namespace fp8moe

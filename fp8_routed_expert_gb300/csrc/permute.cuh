@@ -1,5 +1,5 @@
-// CTA-wide stable counting sort of (token, expert) pairs by expert; used by the
-// standalone permutation kernel and by the fused small-batch routing kernel.
+// Stable counting sort of (token, expert) pairs by expert: CTA-wide (the
+// standalone permutation kernel) and one-warp (the small-batch routing).
 #pragma once
 
 #include "common.cuh"
@@ -126,6 +126,80 @@ __device__ void cta_counting_sort(const int32_t *idx, int64_t P, int E, int tile
     }
     __syncwarp();
     if (valid && (peers & lt_mask) == 0) whist[wid * E + e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// The same sort by ONE warp, for small P (the decode path's few hundred
+// pairs): a compact code path matters more there than parallelism.  Every
+// lane of the calling warp must call it; cur: E ints of shared memory.
+__device__ __forceinline__ void warp_counting_sort(const int32_t *idx, int P, int E, int tile_m,
+                                                   const SortOut &o, int *cur, int *err) {
+  const int lane = threadIdx.x & 31;
+  for (int e = lane; e < E; e += 32) cur[e] = 0;
+  __syncwarp();
+  for (int p = lane; p < P; p += 32) {
+    int e = idx[p];
+    if ((unsigned)e >= (unsigned)E) {
+      set_error(err, DEV_ERR_BOUNDS);
+      e = 0;
+    }
+    atomicAdd(&cur[e], 1);
+  }
+  __syncwarp();
+  // lane l owns experts [l per, (l + 1) per): counts, then scans over lanes
+  const int per = (E + 31) / 32, e0 = lane * per, e1 = e0 + per < E ? e0 + per : E;
+  int c_sum = 0, a_sum = 0, t_sum = 0;
+  for (int e = e0; e < e1; ++e) {
+    const int c = cur[e];
+    c_sum += c;
+    a_sum += c > 0;
+    t_sum += (c + tile_m - 1) / tile_m;
+  }
+  int c_inc = c_sum, a_inc = a_sum, t_inc = t_sum;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int c2 = __shfl_up_sync(0xffffffffu, c_inc, d), a2 = __shfl_up_sync(0xffffffffu, a_inc, d);
+    const int t2 = __shfl_up_sync(0xffffffffu, t_inc, d);
+    if (lane >= d) {
+      c_inc += c2;
+      a_inc += a2;
+      t_inc += t2;
+    }
+  }
+  int off = c_inc - c_sum, act = a_inc - a_sum, toff = t_inc - t_sum;
+  for (int e = e0; e < e1; ++e) {
+    const int c = cur[e];
+    o.counts[e] = c;
+    o.offsets[e] = off;
+    o.tile_offsets[e] = toff;
+    if (c > 0) o.active[act++] = e;
+    cur[e] = off;  // becomes the expert's write cursor
+    off += c;
+    toff += (c + tile_m - 1) / tile_m;
+  }
+  if (lane == 31) {
+    o.offsets[E] = P;
+    o.tile_offsets[E] = t_inc;
+    *o.n_active = a_inc;
+  }
+  __syncwarp();
+  // stable scatter, 32 pairs at a time in pair order
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int base = 0; base < P; base += 32) {
+    const int p = base + lane;
+    const bool valid = p < P;
+    int e = valid ? idx[p] : -1;
+    if (valid && (unsigned)e >= (unsigned)E) e = 0;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt_mask);
+    if (valid) {
+      const int pos = cur[e] + rank;
+      o.perm[pos] = p;
+      o.inv[p] = pos;
+    }
+    __syncwarp();
+    if (valid && rank == 0) cur[e] += __popc(peers);
     __syncwarp();
   }
 }

@@ -466,8 +466,8 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_decode_kernel(
 // ..: it holds the token's logits and bounds in registers (EPL per lane),
 // selects the top k and certifies the order as the general selection does;
 // a token the bound cannot certify goes through the exact path
-// (select_token).  The CTA then sorts the pairs by expert from shared memory
-// and clears the FFN's work counters.
+// (select_token).  Warp 0 then sorts the pairs by expert from shared memory
+// while the other warps clear the FFN's work counters.
 constexpr int kSmallTB = 8;  // tokens per token block
 
 struct RouteSmallArgs {
@@ -707,9 +707,12 @@ __global__ void __launch_bounds__(32 * NW, 1) route_select_small_kernel(RouteSma
       if (lane < k) idx_s[t * k + lane] = a.idx[t * k + lane];
     }
   }
-  for (int i = threadIdx.x; i < r.n_counters; i += blockDim.x) r.counters[i] = 0;
   __syncthreads();
-  cta_counting_sort<NW>(idx_s, T * k, (int)E, r.tile_m, r.so, sort_smem, a.err);
+  if (wid == 0) {
+    warp_counting_sort(idx_s, (int)(T * k), (int)E, r.tile_m, r.so, sort_smem, a.err);
+  } else {
+    for (int i = threadIdx.x - 32; i < r.n_counters; i += blockDim.x - 32) r.counters[i] = 0;
+  }
 }
 
 // f16 copies of every token (the GEMV path above the fused-routing size).
