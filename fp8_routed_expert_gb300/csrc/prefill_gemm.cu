@@ -235,10 +235,19 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.f;
       bool ok = true;
+      const float *sa_p = p.a_scale + (row < p.Pmax ? row : 0);
+      const bool sa_ok = row < p.Pmax;
+      // the scales of K block kb + 1 are loaded while block kb is promoted,
+      // so their latency is not on the path between the MMA and the epilogue
+      float sa_n = sa_ok ? __ldg(sa_p) : 0.f;
+      float s0_n = __ldg(ws + blk0 * nkb), s1_n = __ldg(ws + blk1 * nkb);
       for (int64_t kb = 0; kb < nkb; ++kb) {
-        const float sa = (row < p.Pmax) ? __ldg(p.a_scale + kb * p.Pmax + row) : 0.f;
-        const float c0 = sa * __ldg(ws + blk0 * nkb + kb);
-        const float c1 = sa * __ldg(ws + blk1 * nkb + kb);
+        const float c0 = sa_n * s0_n, c1 = sa_n * s1_n;
+        if (kb + 1 < nkb) {
+          sa_n = sa_ok ? __ldg(sa_p + (kb + 1) * p.Pmax) : 0.f;
+          s0_n = __ldg(ws + blk0 * nkb + kb + 1);
+          s1_n = __ldg(ws + blk1 * nkb + kb + 1);
+        }
         // no early exit on the abort flag here: the epilogue warps share a
         // named barrier, so they must all stop at the same (timed-out) wait
         if (!mbar_wait(&tfull_bar[buf], bphase, nullptr, WAIT_LIMIT_NS)) {
