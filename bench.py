@@ -200,23 +200,35 @@ def oracle_rate(workload: str, seconds: float, max_tokens: int = 64) -> dict:
 
 # ------------------------------------------------------------------ native arm
 
-def kernel_source_sha() -> str:
+# Source files each dominant kernel is compiled from (its .cu file and the
+# headers it includes); a profile's DRAM traffic stays valid while they do not
+# change.
+KERNEL_SOURCES = {
+    "decode_ffn": ("decode_mma.cu", "common.cuh", "kernels.h", "sm100_ptx.cuh"),
+    "grouped_gemm": ("prefill_gemm.cu", "common.cuh", "kernels.h", "sm100_ptx.cuh"),
+    "gemv": ("gemv.cu", "common.cuh", "kernels.h"),
+}
+
+
+def kernel_source_sha(kernel: str | None = None) -> str:
+    """Hash of one kernel's source files (all of csrc/ when kernel is None)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_routed_expert_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    files = KERNEL_SOURCES[kernel] if kernel else os.listdir(csrc)
+    for f in sorted(files):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
-    the current kernel sources."""
+    the kernel's current sources."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     e = d.get(f"{kernel}/{workload}")
-    if not e or e.get("source_sha") != kernel_source_sha():
+    if not e or e.get("source_sha") != kernel_source_sha(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -318,7 +330,7 @@ def run_native(args, rank, local_rank, world):
         dom_bytes = sb["w13"] + sb["w2"] + T * fam.hidden * 2 + P * fam.hidden * 4
         achieved = dom_bytes / dom_s / 1e9
         roof = dict(bound="hbm", achieved=achieved, peak=hbm, unit="GB/s", frac=achieved / hbm,
-                    traffic=profiled_traffic(dominant, args.workload),
+                    traffic=profiled_traffic("decode_ffn", args.workload),
                     kernel="decode_ffn (tcgen05 gate/up + SwiGLU + down, one launch)",
                     algorithmic_bytes=dom_bytes, avg_launch_us=dom_s * 1e6,
                     peak_source=f"hbm_gbs, {src}")
@@ -326,7 +338,7 @@ def run_native(args, rank, local_rank, world):
         dom_bytes = sb["w13"] + T * fam.hidden * 2 + P * fam.inter * 4
         achieved = dom_bytes / dom_s / 1e9
         roof = dict(bound="hbm", achieved=achieved, peak=hbm, unit="GB/s", frac=achieved / hbm,
-                    traffic=profiled_traffic(dominant, args.workload),
+                    traffic=profiled_traffic("gemv", args.workload),
                     kernel="gate_up_swiglu (grouped GEMV)", algorithmic_bytes=dom_bytes,
                     avg_launch_us=dom_s * 1e6, peak_source=f"hbm_gbs, {src}")
     else:
@@ -334,7 +346,7 @@ def run_native(args, rank, local_rank, world):
         fp8_peak = bf16 * FP8_PER_BF16
         achieved = flops / dom_s / 1e12
         roof = dict(bound="tensor", achieved=achieved, peak=fp8_peak, unit="TFLOP/s",
-                    frac=achieved / fp8_peak, traffic=profiled_traffic(dominant, args.workload),
+                    frac=achieved / fp8_peak, traffic=profiled_traffic("grouped_gemm", args.workload),
                     kernel="gate_up_swiglu (grouped GEMM)", algorithmic_flops=flops,
                     avg_launch_us=dom_s * 1e6,
                     peak_source=f"bf16_tflops x {FP8_PER_BF16} (nominal fp8/bf16), {src}")

@@ -131,8 +131,11 @@ __device__ __forceinline__ double exact_logit(const SelectArgs &a, const __nv_bf
 // Top-k of token t by one warp.  Per-warp shared memory: lg and bt (E floats
 // each: logits + bias and their error bounds) and lg64 (E doubles).  Logits
 // are read with ld.global.cg so that planes written by other CTAs of the same
-// grid are seen.
-__device__ void select_token(const SelectArgs &a, int64_t t, float xn, float *lg, float *bt,
+// grid are seen.  Kept out of line: the small-batch selection calls it only
+// for tokens its bound cannot certify, and a launch that follows an L2 flush
+// pays for every instruction line it fetches, so this code stays off that
+// kernel's common path.
+__device__ __noinline__ void select_token(const SelectArgs &a, int64_t t, float xn, float *lg, float *bt,
                              double *lg64) {
   const int lane = threadIdx.x & 31;
   const int E = (int)a.E, k = a.k;
