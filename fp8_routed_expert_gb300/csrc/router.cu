@@ -105,7 +105,7 @@ __device__ __forceinline__ void x_to_f16(const __nv_bfloat16 *xt, int64_t H, flo
 __device__ __forceinline__ double exact_logit(const SelectArgs &a, const __nv_bfloat16 *xt, int e) {
   const int lane = threadIdx.x & 31;
   const float *w = a.W + (int64_t)e * a.H;
-  double acc = 0.0;
+  double acc[4] = {0.0, 0.0, 0.0, 0.0};  // independent chains: the f64 pipe is slow
   for (int64_t h0 = 4 * lane; h0 < a.H; h0 += 512) {
     float4 wv[4];
     uint2 xv[4];
@@ -117,13 +117,13 @@ __device__ __forceinline__ double exact_logit(const SelectArgs &a, const __nv_bf
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      acc = fma((double)bf16_bits_to_float(xv[u].x & 0xffffu), (double)wv[u].x, acc);
-      acc = fma((double)bf16_bits_to_float(xv[u].x >> 16), (double)wv[u].y, acc);
-      acc = fma((double)bf16_bits_to_float(xv[u].y & 0xffffu), (double)wv[u].z, acc);
-      acc = fma((double)bf16_bits_to_float(xv[u].y >> 16), (double)wv[u].w, acc);
+      acc[u] = fma((double)bf16_bits_to_float(xv[u].x & 0xffffu), (double)wv[u].x, acc[u]);
+      acc[u] = fma((double)bf16_bits_to_float(xv[u].x >> 16), (double)wv[u].y, acc[u]);
+      acc[u] = fma((double)bf16_bits_to_float(xv[u].y & 0xffffu), (double)wv[u].z, acc[u]);
+      acc[u] = fma((double)bf16_bits_to_float(xv[u].y >> 16), (double)wv[u].w, acc[u]);
     }
   }
-  double v = warp_sum(acc);
+  double v = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
   if (a.bias != nullptr) v += (double)a.bias[e];
   return v;
 }
@@ -745,9 +745,11 @@ __global__ void __launch_bounds__(128) router_select_kernel(SelectArgs a) {
 
 // ------------------------------------------------------------------ logits, T large
 // Tiled SIMT product: a CTA computes 64 tokens x 64 experts, each thread a
-// 4 x 4 block.  Each 128-wide K block is summed into a fresh partial by a
-// chain of 128 fma, then added to the running total: rounding chain length
-// 128 + H/128 (+1 for the bias).
+// 4 x 4 block.  Every 32 columns are summed into a fresh partial by a chain
+// of 32 fma; the four partials of a 128-wide K block are added into the
+// block's sum, which is added to the running total: rounding chain length
+// 32 + 4 + H/128 (+ the planes' sum and the bias).  Short chains keep the
+// error bound, and with it the share of tokens sent to the exact path, small.
 __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
     const __nv_bfloat16 *__restrict__ x, int64_t T, const float *__restrict__ W, int64_t E,
     int64_t H, float *__restrict__ logits) {
@@ -771,11 +773,16 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
   const int lr = tid >> 2;        // row of the tile this thread stages (0..63)
   const int lk = (tid & 3) * 8;   // first of its 8 k values
   for (int64_t kb = kb_lo * 128; kb < kb_hi * 128; kb += 128) {
+    float blk[4][4];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
+      for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
     for (int kt = 0; kt < 128; kt += 32) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
       const int64_t k0 = kb + kt + lk;
       {
         float v[8];
@@ -817,11 +824,15 @@ __global__ void __launch_bounds__(256) router_logits_tiled_kernel(
           for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
       }
       __syncthreads();
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) blk[i][j] += part[i][j];
     }
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) tot[i][j] += part[i][j];
+      for (int j = 0; j < 4; ++j) tot[i][j] += blk[i][j];
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -867,7 +878,7 @@ int router_k_split(int64_t T, int64_t E, int64_t H, int sms) {
 
 int router_chain_depth(int64_t T, int64_t H, int ks) {
   return T <= kRouterWarpMaxT ? (int)(4 * ((H + 1023) / 1024) + 5 + 8 + 1)
-                              : (int)(128 + H / 128 + ks + 1);
+                              : (int)(32 + 4 + H / 128 + ks + 1);
 }
 
 float router_gamma(int64_t T, int64_t H, int ks) {
