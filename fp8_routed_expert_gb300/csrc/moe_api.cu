@@ -79,15 +79,15 @@ int check_config(const moe_config *c) {
   return MOE_OK;
 }
 
-// Events around one kernel launch when timing is on.
+// Events around one step's launches (n_kernels kernels) when timing is on.
 struct Timed {
   moe_ctx *c;
   int kernel;
   cudaStream_t s;
   cudaEvent_t a = nullptr, b = nullptr;
   bool on;
-  Timed(moe_ctx *ctx, int k, cudaStream_t st) : c(ctx), kernel(k), s(st) {
-    c->n_launches += 1;
+  Timed(moe_ctx *ctx, int k, cudaStream_t st, int n_kernels = 1) : c(ctx), kernel(k), s(st) {
+    c->n_launches += n_kernels;
     on = (c->timing >> k) & 1;
     if (!on) return;
     a = take();
@@ -148,7 +148,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
   if (path == MOE_PATH_TCGEMV) {
     const int64_t max_tiles = (P + kDecodeTileN - 1) / kDecodeTileN + max_active;
     if (T <= kRouterWarpMaxT) {
-      Timed tm(c, MOE_K_ROUTE, s);
+      Timed tm(c, MOE_K_ROUTE, s, 2);  // logits, then selection + sort
       CUDA_TRY(launch_route_small(x, T, rw, rb, E, H, k, c->logits, c->wnorm, c->xss, c->a_hi,
                                   c->a_lo, c->a_scale, Pm, c->done13, (int)max_tiles + 1,
                                   c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv, c->active,
@@ -156,7 +156,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
     } else {
       const int ks = router_k_split(T, E, H, c->sms);
       {
-        Timed tm(c, MOE_K_ROUTER_LOGITS, s);
+        Timed tm(c, MOE_K_ROUTER_LOGITS, s, 2);  // row norms, then the tiled logits
         CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
       }
       {
@@ -211,7 +211,7 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
                                  path == MOE_PATH_GEMV ? c->hmax : nullptr, c->err, s));
   } else {
     {
-      Timed tm(c, MOE_K_ROUTER_LOGITS, s);
+      Timed tm(c, MOE_K_ROUTER_LOGITS, s, 2);  // row norms, then the tiled logits
       CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
     }
     {
@@ -219,7 +219,10 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
       CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks, gamma, c->idx,
                                     c->wts, c->err, s));
     }
-    if (path == MOE_PATH_GEMV) CUDA_TRY(launch_x_to_f16(x, T, H, c->x16, c->xscale, s));
+    if (path == MOE_PATH_GEMV) {
+      c->n_launches += 1;
+      CUDA_TRY(launch_x_to_f16(x, T, H, c->x16, c->xscale, s));
+    }
     {
       Timed tm(c, MOE_K_PERMUTE, s);
       CUDA_TRY(launch_permute(c->idx, P, (int)E, tile_m, c->counts, c->offsets, c->perm, c->inv,

@@ -309,7 +309,8 @@ def test_kernel_timing_api():
     for _ in range(3):
         run(layer, x, dw, fam.top_k)
     assert layer.resolved_path(8) == "tcgemv"
-    assert layer.launch_count() - n0 == 3 * 3   # routing, fused gate/up + down, combine
+    # routing logits, selection + sort, fused gate/up + down, combine
+    assert layer.launch_count() - n0 == 3 * 4
     for name in ("route", "gate_up", "combine"):
         ms, n = layer.kernel_time(name)
         assert n == 3 and ms > 0, name
