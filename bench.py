@@ -17,6 +17,8 @@ Printed: ONE JSON line.  Besides the contract keys it carries
   layer         : the same for the whole step (selected-expert bytes / step);
   cpu_baseline  : the f64 CPU oracle on a bounded sample of the workload;
   e2e           : the metric through the host-buffer C-ABI entry point;
+  kernels_us    : per-kernel-step CUDA-event times from a few extra steps
+                  after the timed region (events between the kernels);
   clocks        : nvidia-smi samples taken during the timed region.
 ``--impl reference`` times the CPU oracle as the reference arm instead.
 Under torchrun (N > 1) every rank runs an independent replica.
@@ -42,6 +44,9 @@ import workloads as W  # noqa: E402
 METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill FP8 TFLOP/s vs roofline"
 UNIT = "tokens/s"
 DEFAULT_WORKLOAD = "olmoe_decode_T8"
+# the library's timed kernel steps (a step may be two chained kernels)
+KERNEL_STEPS = ("route", "router_logits", "router_select", "permute", "act_quant", "gate_up",
+                "down", "combine")
 FLUSH_BYTES = 256 << 20
 FP8_PER_BF16 = 2.0  # nominal dense FP8 / BF16 tensor throughput on GB300 (4.5 / 2.25 PFLOP/s)
 
@@ -233,6 +238,33 @@ def profiled_traffic(kernel: str, workload: str):
     return e.get("dram_bytes_per_launch")
 
 
+def kernel_breakdown(layer, step, flush, dev, n: int):
+    """Average CUDA-event time (us) of each kernel step of the layer over n
+    extra steps after the timed region (L2 flushed before each).  Events sit
+    between the kernels, so the chained launches lose their overlap here; the
+    timed region above has no such events.  None if the timing API fails."""
+    import torch
+    try:
+        layer.set_timing("all")
+        for _ in range(n):
+            flush()
+            step()
+        torch.cuda.synchronize(dev)
+        out = {}
+        for name in KERNEL_STEPS:
+            ms, c = layer.kernel_time(name)
+            if c:
+                out[name] = round(ms / c * 1e3, 2)
+        layer.set_timing(())
+        return out
+    except Exception as e:  # the breakdown is auxiliary: never lose the bench line for it
+        try:
+            layer.set_timing(())
+        except Exception:
+            pass
+        return {"unavailable": str(e)[:200]}
+
+
 def run_native(args, rank, local_rank, world):
     import torch
     import __graft_entry__
@@ -298,6 +330,8 @@ def run_native(args, rank, local_rank, world):
     layer.set_timing(())
     assert layer.status() == 0
     step_ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / K
+
+    kernels_us = kernel_breakdown(layer, step, flush, dev, 20 if decode else 5)
 
     # end to end through the host-buffer entry point (pinned buffers)
     xh = torch.from_numpy(xb.astype(np.int16)).view(torch.bfloat16).pin_memory()
@@ -372,6 +406,7 @@ def run_native(args, rank, local_rank, world):
         "layer": {"bytes": layer_bytes, "gbs": layer_gbs, "hbm_frac": layer_gbs / hbm,
                   "expert_tflops": expert_flops / (step_ms / 1e3) / 1e12},
         "gpu_launches": int(launches),
+        "kernels_us": kernels_us,
         "e2e": {"value": job_throughput(world, T, e2e_step), "unit": UNIT,
                 "h2d_bytes_per_step": T * fam.hidden * 2, "d2h_bytes_per_step": T * fam.hidden * 2,
                 "ms_per_step": e2e_step},

@@ -60,3 +60,33 @@ def test_selected_bytes_count_active_experts_only():
     per2 = H * I + 4 * (H // 128) * (I // 128)
     assert sb["w13"] == 3 * per13 and sb["w2"] == 3 * per2
     assert sb["w13"] + sb["w2"] == 3 * fam.expert_bytes
+
+
+class _FakeLayer:
+    """Stands in for MoELayer's timing API: two kernel steps were timed."""
+
+    def __init__(self, fail=False):
+        self.mask, self.fail, self.steps = None, fail, 0
+
+    def set_timing(self, kernels=()):
+        if self.fail and kernels:
+            raise RuntimeError("timing unavailable")
+        self.mask = kernels
+
+    def kernel_time(self, name):
+        return {"gate_up": (2.0, 4), "combine": (0.04, 4)}.get(name, (0.0, 0))
+
+
+def test_kernel_breakdown(monkeypatch):
+    import torch
+    monkeypatch.setattr(torch.cuda, "synchronize", lambda *a: None)
+    layer = _FakeLayer()
+    calls = []
+    out = bench.kernel_breakdown(layer, lambda: calls.append("step"), lambda: calls.append("flush"),
+                                 None, 4)
+    assert out == {"gate_up": 500.0, "combine": 10.0}
+    assert calls == ["flush", "step"] * 4
+    assert layer.mask == ()  # timing switched off again
+    bad = _FakeLayer(fail=True)
+    out = bench.kernel_breakdown(bad, lambda: None, lambda: None, None, 2)
+    assert "unavailable" in out and bad.mask == ()
