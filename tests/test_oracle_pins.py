@@ -204,6 +204,35 @@ def test_oracle_agrees_with_independent_torch_f64():
     assert _rel(res["out"], out.numpy()) < 1e-10
 
 
+def test_one_expert_is_the_dense_ffn():
+    """With one expert and k = 1 the layer is a dense SwiGLU FFN in the same
+    blockwise-FP8 format (dragon.c, "Precision": the dense branches share the
+    routed experts' format): every token has weight exactly 1, the permutation
+    is the identity, and the output is bf16(W2 (silu(W1 x) * (W3 x))), here
+    through torch's decode table and f64 matmuls."""
+    fam = W.family("dense_ffn")
+    assert fam.n_experts == 1 and fam.top_k == 1
+    w = W.make_weights(fam)
+    T = 4
+    x = W.make_x(fam, fam.tokens[0])[:T]
+    res = oracle.moe_forward(x, w.router_w, None, w.w13, w.s13, w.w2, w.s2, 1)
+    assert (res["idx"] == 0).all() and (res["wts"] == 1.0).all()
+    assert res["counts"].tolist() == [T] and res["perm"].tolist() == list(range(T))
+    dec = torch.tensor(_torch_decode_table(), dtype=torch.float64)
+    I = fam.inter
+    s13 = torch.from_numpy(w.s13[0]).double().repeat_interleave(128, 0).repeat_interleave(128, 1)
+    s2 = torch.from_numpy(w.s2[0]).double().repeat_interleave(128, 0).repeat_interleave(128, 1)
+    w13 = dec[torch.from_numpy(w.w13[0]).long()] * s13
+    w2 = dec[torch.from_numpy(w.w2[0]).long()] * s2
+    xt = torch.from_numpy(x.astype(np.int16)).view(torch.bfloat16).double()
+    dense = (torch.nn.functional.silu(xt @ w13[:I].T) * (xt @ w13[I:].T)) @ w2.T
+    assert _rel(res["out"], dense.numpy()) < 1e-10
+    want = dense.to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    # one rounding of the f64 sum; the float32 detour may double-round only
+    # where f64 lies within 2^-29 relative of a bf16 midpoint
+    assert (oracle.round_to_bf16(res["out"]) != want).mean() < 1e-3
+
+
 # ----------------------------------------------------------------------------- invariants
 
 @pytest.mark.parametrize("name,T", [("tiny", 4), ("olmoe_decode", 8), ("olmoe_prefill", 64)])

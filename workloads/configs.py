@@ -11,11 +11,16 @@ Shapes and value distributions of the five workload families:
                     top-6 routing of the DeepSeek-V4.1-Flash post)
 * ``large_prefill`` T=4096, H=6144, E=512, top-12, I=2048, router bias ~N(0, 1):
                     heavy imbalance with experts that receive no token
+* ``dense_ffn``     T in {8, 2048}, H=2048, one expert, top-1, I=8192: a dense
+                    (or shared-expert) SwiGLU FFN in the same blockwise-FP8
+                    format (dragon.c, "Precision": the per-sub-block dense
+                    branches are e4m3 with 128x128 f32 block scales too); with
+                    one expert the router gives every token weight 1
 
 All families draw x ~ N(0,1) rounded to bf16, router W ~ N(0, 0.02) in f32, and
 expert weights ~ N(0, 0.02) quantised to e4m3 with one f32 scale per 128x128
 block (the dragon.c page, "Precision").  Seeds: tiny 1, olmoe_decode 2,
-olmoe_prefill 3, wide_decode 4, large_prefill 5; the activations of a T-token
+olmoe_prefill 3, wide_decode 4, large_prefill 5, dense_ffn 6; the activations of a T-token
 batch use seed*1000 + T so that each T has its own batch.
 """
 from __future__ import annotations
@@ -52,6 +57,7 @@ FAMILIES = {
     "olmoe_prefill": Family("olmoe_prefill", 2048, 64, 8, 1024, 3, (512, 2048), bias_std=0.5),
     "wide_decode": Family("wide_decode", 4096, 384, 6, 2048, 4, (1, 16, 64)),
     "large_prefill": Family("large_prefill", 6144, 512, 12, 2048, 5, (4096,), bias_std=1.0),
+    "dense_ffn": Family("dense_ffn", 2048, 1, 1, 8192, 6, (8, 2048)),
 }
 
 # tensor ids of the counter-based streams
