@@ -8,14 +8,21 @@ A step is one pass of the whole layer (router, permutation, gate/up + SwiGLU,
 down, combine) over one synthetic batch already resident in HBM.  The L2 is
 flushed before every step (a 256 MiB memset, twice the 129 MB L2, then a
 read of another 256 MiB so that no dirty line of the memset is left to be
-written back inside the timed step) and the step is timed with CUDA events on the launching stream.  The default workload
-is the OLMoE-shaped decode batch of 8 tokens (H=2048, E=64, top-8, I=1024).
+written back inside the timed step) and the step is timed with CUDA events
+on the launching stream.  The default workload is the largest single-GPU
+configuration, the large prefill batch (T=4096, H=6144, E=512, top-12,
+I=2048, router bias N(0, 1)); ``--workload`` selects the others (e.g.
+olmoe_decode_T8, olmoe_prefill_T2048, wide_decode_T64).
 
 Printed: ONE JSON line.  Besides the contract keys it carries
   roofline      : the dominant kernel's algorithmic bytes (or FLOPs) per launch
-                  over its CUDA-event duration, against MEASURED_PEAKS.json;
+                  over its CUDA-event duration, against MEASURED_PEAKS.json
+                  (the gate/up GEMM on prefill batches also gives its FP8
+                  TFLOP/s and the attainable fraction max(bytes / bandwidth,
+                  FLOPs / FP8 peak) / time);
   layer         : the same for the whole step (selected-expert bytes / step);
-  cpu_baseline  : the f64 CPU oracle on a bounded sample of the workload;
+  cpu_baseline  : the f64 CPU oracle, threaded over tokens (router) and expert
+                  segments (FFN) on all host cores, on a bounded sample;
   e2e           : the metric through the host-buffer C-ABI entry point;
   kernels_us    : per-kernel-step CUDA-event times from a few extra steps
                   after the timed region (events between the kernels);
@@ -32,6 +39,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -43,7 +51,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "MoE-layer tokens/s; decode HBM GB/s & prefill FP8 TFLOP/s vs roofline"
 UNIT = "tokens/s"
-DEFAULT_WORKLOAD = "olmoe_decode_T8"
+DEFAULT_WORKLOAD = "large_prefill_T4096"
 # the library's timed kernel steps (a step may be two chained kernels)
 KERNEL_STEPS = ("route", "router_logits", "router_select", "permute", "act_quant", "gate_up",
                 "down", "combine")
@@ -114,11 +122,11 @@ class ClockSampler:
     def __init__(self, device: int):
         self.device = device
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{device}.csv")
+        fd, self.path = tempfile.mkstemp(prefix=f"clocks_dev{device}_", suffix=".csv")
+        os.close(fd)
 
     def __enter__(self):
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -155,6 +163,10 @@ class ClockSampler:
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
@@ -163,44 +175,65 @@ class ClockSampler:
 
 # ------------------------------------------------------------------ oracle timing
 
+def oracle_sample_tokens(fam, T: int) -> int:
+    """Tokens of the oracle's bounded sample: the first n tokens of the batch,
+    run through the whole layer.  The oracle dequantises every expert the
+    sample touches, so the sample is smaller for the large experts."""
+    return min(T, 64 if fam.expert_bytes <= (8 << 20) else 8)
+
+
 _ORACLE_CHILD = r"""
-import json, sys, time, os
+import json, os, sys, time
 sys.path.insert(0, sys.argv[1])
 import numpy as np
-import workloads as W, oracle
+import workloads as W
+from oracle import threaded
 fam, T = W.parse_workload(sys.argv[2])
-budget, max_tokens = float(sys.argv[3]), int(sys.argv[4])
+budget, n, reps_max, warm = float(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5]), int(sys.argv[6])
 w = W.make_weights(fam)
-x = W.make_x(fam, T)
-tokens = np.arange(min(T, max_tokens))
-t0 = time.perf_counter(); n = 0
+x = W.make_x(fam, T)[:n]
+run = lambda: threaded.moe_forward(x, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2,
+                                   fam.top_k)
+for _ in range(warm):
+    run()
+times = []
+t0 = time.perf_counter()
 while True:
-    oracle.moe_forward(x, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2, fam.top_k,
-                       tokens=tokens)
-    n += 1
-    el = time.perf_counter() - t0
-    if el >= budget or n >= 1000:
+    a = time.perf_counter(); run(); times.append(time.perf_counter() - a)
+    if len(times) >= reps_max or (budget > 0 and time.perf_counter() - t0 >= budget):
         break
-print(json.dumps({"seconds": el, "reps": n, "tokens_per_rep": int(tokens.size), "T": T}))
+print(json.dumps({"times": times, "n": n, "T": T, "cores": threaded.default_workers()}))
 """
 
 
-def oracle_rate(workload: str, seconds: float, max_tokens: int = 64) -> dict:
-    """Oracle tokens/s on the host cores, in a fresh single-threaded process.
-
-    Sample: the whole routing of the batch plus the expert FFN and combine of
-    its first min(T, max_tokens) tokens, repeated for about `seconds`."""
+def _oracle_child(workload: str, budget: float, reps_max: int, warm: int) -> dict:
+    fam, T = W.parse_workload(workload)
+    n = oracle_sample_tokens(fam, T)
+    # one expert per thread, each with a single-threaded BLAS
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-c", _ORACLE_CHILD, ROOT, workload, str(seconds),
-                        str(max_tokens)], capture_output=True, text=True, env=env, timeout=1800)
+    r = subprocess.run([sys.executable, "-c", _ORACLE_CHILD, ROOT, workload, str(budget), str(n),
+                        str(reps_max), str(warm)], capture_output=True, text=True, env=env,
+                       timeout=3600)
     if r.returncode != 0:
-        raise RuntimeError("oracle timing failed: " + r.stderr[-2000:])
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    rate = d["reps"] * d["tokens_per_rep"] / d["seconds"]
-    return dict(value=rate, unit=UNIT, cores=1, kind="oracle",
-                sample=(f"{d['reps']} oracle passes over {workload}: routing of all {d['T']} tokens "
-                        f"+ experts and combine of {d['tokens_per_rep']} tokens, f64, "
-                        f"{d['seconds']:.1f} s"), seconds=d["seconds"])
+        raise RuntimeError("oracle run failed: " + r.stderr[-2000:])
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def _oracle_sample_text(workload: str, d: dict) -> str:
+    return (f"whole layer (routing, experts, combine) on the first {d['n']} of the "
+            f"{d['T']} tokens of {workload}, f64 oracle threaded over tokens (router) and "
+            f"expert segments (FFN) on {d['cores']} host threads; every expert the sample "
+            f"touches is dequantised once per pass")
+
+
+def oracle_rate(workload: str, seconds: float) -> dict:
+    """Oracle tokens/s on all host cores: passes over the bounded sample for
+    about `seconds`, in a fresh process."""
+    d = _oracle_child(workload, seconds, 1000, 0)
+    el = sum(d["times"])
+    return dict(value=len(d["times"]) * d["n"] / el, unit=UNIT, cores=d["cores"], kind="oracle",
+                sample=f"{len(d['times'])} passes, {el:.1f} s: " + _oracle_sample_text(workload, d),
+                seconds=el)
 
 
 # ------------------------------------------------------------------ native arm
@@ -236,6 +269,36 @@ def profiled_traffic(kernel: str, workload: str):
     if not e or e.get("source_sha") != kernel_source_sha(kernel):
         return None
     return e.get("dram_bytes_per_launch")
+
+
+def gemm1_roofline(fam, T: int, sb: dict, launch_s: float, hbm_gbs: float, fp8_tflops: float,
+                   peak_src: str) -> dict:
+    """Roofline of the gate/up grouped GEMM (one launch, launch_s seconds).
+
+    Algorithmic FLOPs 2 P H 2I; algorithmic bytes = the selected experts' W13
+    codes and scales + x (bf16).  Its floor is the larger of bytes / HBM
+    bandwidth and FLOPs / FP8 peak; ``bound`` names that side and ``achieved``
+    / ``peak`` / ``frac`` are given on it, with the other side beside them
+    (``tflops`` / ``fp8_frac`` and ``gbs`` / ``hbm_frac``) and
+    ``attainable_frac`` = floor / time."""
+    P = T * fam.top_k
+    flops = 2.0 * P * fam.hidden * 2 * fam.inter
+    nbytes = sb["w13"] + T * fam.hidden * 2
+    tflops = flops / launch_s / 1e12
+    gbs = nbytes / launch_s / 1e9
+    t_hbm, t_tc = nbytes / (hbm_gbs * 1e9), flops / (fp8_tflops * 1e12)
+    r = dict(kernel="gate_up_swiglu (grouped GEMM)", algorithmic_flops=flops,
+             algorithmic_bytes=nbytes, avg_launch_us=launch_s * 1e6,
+             tflops=tflops, fp8_peak_tflops=fp8_tflops, fp8_frac=tflops / fp8_tflops,
+             gbs=gbs, hbm_frac=gbs / hbm_gbs, attainable_frac=max(t_hbm, t_tc) / launch_s,
+             peak_source=(f"hbm_gbs and bf16_tflops x {FP8_PER_BF16} (nominal fp8/bf16), "
+                          f"{peak_src}"))
+    if t_hbm >= t_tc:
+        r.update(bound="hbm", achieved=gbs, peak=hbm_gbs, unit="GB/s", frac=gbs / hbm_gbs)
+    else:
+        r.update(bound="tensor", achieved=tflops, peak=fp8_tflops, unit="TFLOP/s",
+                 frac=tflops / fp8_tflops)
+    return r
 
 
 def kernel_breakdown(layer, step, flush, dev, n: int):
@@ -376,17 +439,13 @@ def run_native(args, rank, local_rank, world):
                     kernel="gate_up_swiglu (grouped GEMV)", algorithmic_bytes=dom_bytes,
                     avg_launch_us=dom_s * 1e6, peak_source=f"hbm_gbs, {src}")
     else:
-        flops = 2.0 * P * fam.hidden * 2 * fam.inter
-        fp8_peak = bf16 * FP8_PER_BF16
-        achieved = flops / dom_s / 1e12
-        roof = dict(bound="tensor", achieved=achieved, peak=fp8_peak, unit="TFLOP/s",
-                    frac=achieved / fp8_peak, traffic=profiled_traffic("grouped_gemm", args.workload),
-                    kernel="gate_up_swiglu (grouped GEMM)", algorithmic_flops=flops,
-                    avg_launch_us=dom_s * 1e6,
-                    peak_source=f"bf16_tflops x {FP8_PER_BF16} (nominal fp8/bf16), {src}")
+        roof = gemm1_roofline(fam, T, sb, dom_s, hbm, bf16 * FP8_PER_BF16, src)
+        roof["traffic"] = profiled_traffic("grouped_gemm", args.workload)
     layer_bytes = sb["w13"] + sb["w2"] + sb["router"] + 2 * T * fam.hidden * 2
     layer_gbs = layer_bytes / (step_ms / 1e3) / 1e9
     expert_flops = 6.0 * P * fam.hidden * fam.inter
+    fp8_peak = bf16 * FP8_PER_BF16
+    layer_floor_s = max(layer_bytes / (hbm * 1e9), expert_flops / (fp8_peak * 1e12))
     value = job_throughput(world, T, step_ms)
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -404,7 +463,9 @@ def run_native(args, rank, local_rank, world):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "roofline": roof,
         "layer": {"bytes": layer_bytes, "gbs": layer_gbs, "hbm_frac": layer_gbs / hbm,
-                  "expert_tflops": expert_flops / (step_ms / 1e3) / 1e12},
+                  "expert_tflops": expert_flops / (step_ms / 1e3) / 1e12,
+                  "expert_fp8_frac": expert_flops / (step_ms / 1e3) / 1e12 / fp8_peak,
+                  "attainable_frac": layer_floor_s / (step_ms / 1e3)},
         "gpu_launches": int(launches),
         "kernels_us": kernels_us,
         "e2e": {"value": job_throughput(world, T, e2e_step), "unit": UNIT,
@@ -449,48 +510,25 @@ def main():
     return 0
 
 
-_REF_STEP = r"""
-import json, sys, time
-sys.path.insert(0, sys.argv[1])
-import numpy as np
-import workloads as W, oracle
-fam, T = W.parse_workload(sys.argv[2])
-steps, warm, max_tokens = int(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5])
-w = W.make_weights(fam)
-x = W.make_x(fam, T)
-tokens = np.arange(min(T, max_tokens))
-times = []
-for i in range(warm + steps):
-    t0 = time.perf_counter()
-    oracle.moe_forward(x, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2, fam.top_k,
-                       tokens=tokens)
-    if i >= warm:
-        times.append(time.perf_counter() - t0)
-print(json.dumps({"times": times, "tokens": int(tokens.size), "T": T}))
-"""
-
-
-def oracle_reference_arm(workload: str, steps: int, warmup: int, max_tokens: int = 64) -> dict:
+def oracle_reference_arm(workload: str, steps: int, warmup: int) -> dict:
     """The reference arm: the CPU oracle timed on the host cores, one bounded
-    sample of the workload per step (routing of the whole batch, experts and
-    combine of its first min(T, 64) tokens)."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    r = subprocess.run([sys.executable, "-c", _REF_STEP, ROOT, workload, str(steps), str(warmup),
-                        str(max_tokens)], capture_output=True, text=True, env=env, timeout=3600)
-    if r.returncode != 0:
-        return {"impl": "reference", "unavailable": "oracle run failed: " + r.stderr[-300:]}
-    d = json.loads(r.stdout.strip().splitlines()[-1])
-    sec = sum(d["times"]) / len(d["times"])
-    value = d["tokens"] / sec
+    sample of the workload per step (the whole layer on the batch's first
+    tokens, threaded over tokens and expert segments)."""
+    try:
+        d = _oracle_child(workload, 0.0, steps, warmup)
+    except Exception as e:  # noqa: BLE001
+        return {"impl": "reference", "unavailable": str(e)[-300:]}
+    times = d["times"][:steps]
+    sec = sum(times) / len(times)
+    value = d["n"] / sec
     fam, T = W.parse_workload(workload)
-    sample = (f"per step: routing of all {d['T']} tokens + experts and combine of "
-              f"{d['tokens']} tokens of {workload}, f64 oracle, 1 thread")
+    sample = "per step: " + _oracle_sample_text(workload, d)
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": workload, "tokens": T, "hidden": fam.hidden,
                        "experts": fam.n_experts, "top_k": fam.top_k, "inter": fam.inter},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": d["cores"], "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}

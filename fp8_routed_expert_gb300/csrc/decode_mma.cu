@@ -29,8 +29,9 @@
 // Work queue.  The items form one list: every gate/up item (tile-major), then
 // every down item (tile-major).  CTAs take items from a global counter, one
 // at a time, so that a CTA that finishes early takes more and the tail is at
-// most one item long.  CTA b starts with item b; the counter hands out the
-// rest (item = grid size + counter).  The weight producer takes the next item
+// most one item long.  Every item, a CTA's first included, comes from the
+// counter, so an item belongs only to a CTA that is already running (a CTA
+// that is not yet resident holds none).  The weight producer takes the next item
 // when it issues the last load of the current one and hands its index to the
 // other roles through a small ring in shared memory.
 // A down item needs h of its tile, i.e. every gate/up item of the tile
@@ -100,7 +101,7 @@ struct FfnArgs {
   float *y;                               // three term planes [3][y_plane]: [P, H] each
   int64_t y_plane;
   int32_t *done13;                        // finished gate/up items per tile (0 at entry)
-  int32_t *queue;                         // items handed out beyond the first grid-size ones (0 at entry)
+  int32_t *queue;                         // items handed out so far (0 at entry)
   int *err;
 };
 
@@ -293,7 +294,9 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
     }
     int stage = 0, slot = 0;
     uint32_t phase = 0, qphase = 0;
-    int64_t item = blockIdx.x;  // the first item of every CTA is its index; the queue counts the rest
+    int64_t item = 0;  // every item comes from the queue, the first one included
+    if (lane == 0) item = atomicAdd(p.queue, 1);
+    item = __shfl_sync(0xffffffffu, item, 0);
     bool run = true;
     while (run) {
       // hand the item to the other roles
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
         }
         if (lane == 0) {
           // the next item is taken with the last load of this one
-          if (kb == nkb - 1) next = (int)gridDim.x + atomicAdd(p.queue, 1);
+          if (kb == nkb - 1) next = atomicAdd(p.queue, 1);
           uint8_t *sb = smem + (size_t)stage * STAGE + A_BYTES;
           mbar_arrive_expect_tx(&full_b[stage], B_BYTES);
           const int32_t kx = (int32_t)(kb * BK);

@@ -1,7 +1,12 @@
 import os
 import sys
 
-import pytest
+# The oracle's thread pool (oracle/threaded.py) runs one expert per thread;
+# a multi-threaded BLAS inside every thread would oversubscribe the cores.
+# Must be set before numpy is first imported.
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+
+import pytest  # noqa: E402
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:

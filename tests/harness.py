@@ -18,10 +18,15 @@ import torch
 import oracle
 import workloads as W
 from fp8_routed_expert_gb300 import MoELayer
+from oracle import threaded
 
 REL_L2 = 1e-2
 MAXABS_RMS = 2e-2
 WTS_ATOL = 2e-5
+# y of the tensor-core paths against the oracle's y (relative L2 per expert):
+# x enters exactly (two e4m3 terms), h with about 12 bits (three terms), so y
+# stays near 1e-5; the bound leaves an order of magnitude.
+Y_REL_L2 = 2e-4
 
 DEV = torch.device("cuda", 0)
 
@@ -66,6 +71,54 @@ def run(layer: MoELayer, x_bits: np.ndarray, dw: DeviceWeights, k: int, path: st
 def reference(x_bits, w: W.LayerWeights, k: int, tokens=None, keep_h=False):
     return oracle.moe_forward(x_bits, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2, k,
                               tokens=tokens, keep_h=keep_h)
+
+
+def reference_threaded(x_bits, w: W.LayerWeights, k: int, tokens=None):
+    """The oracle with its per-token and per-expert loops on all host cores
+    (identical results to ``reference``)."""
+    return threaded.moe_forward(x_bits, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2, k,
+                                tokens=tokens)
+
+
+def oracle_expert_y(x_bits, w: W.LayerWeights, idx, experts) -> dict:
+    """The oracle's y of every position of each expert in ``experts``, in
+    position order (ascending pair id), from the oracle's own routing idx."""
+    x = oracle.bf16_to_f64(x_bits)
+    seg = threaded.expert_segments(x, idx, experts, w.w13, w.s13, w.w2, w.s2)
+    return {e: v[3] for e, v in seg.items()}
+
+
+def gpu_y(layer: MoELayer, P: int, H: int, path: str) -> torch.Tensor:
+    """y of the last forward in position order, f32 [P, H] on the device (the
+    sum of the three term planes on the tensor-core decode path)."""
+    if path == "tcgemv":
+        y3 = layer.debug_buffer("y_terms", torch.float32, (3, P, H))
+        return y3[0] + y3[1] + y3[2]
+    return layer.debug_buffer("y", torch.float32, (P, H))
+
+
+def tile_class_experts(counts: np.ndarray, tile: int) -> list:
+    """Experts whose segments cover the tile classes: the busiest, one whose
+    count is 1 mod the tile (else the nearest above it), the smallest non-empty
+    one, one in the middle of the active list and the last non-empty one."""
+    act = np.nonzero(counts > 0)[0]
+    pick = [int(act[np.argmax(counts[act])]), int(act[np.argmin(counts[act])]),
+            int(act[len(act) // 2]), int(act[-1])]
+    rem = (counts[act] - 1) % tile
+    pick.append(int(act[np.argmin(rem)]))
+    return sorted(set(pick))
+
+
+def check_expert_y(y_gpu_rows: np.ndarray, y_ref: np.ndarray, what: str = ""):
+    """Relative L2 <= Y_REL_L2 and max |error| <= MAXABS_RMS x RMS over one
+    expert's positions."""
+    diff = y_gpu_rows - y_ref
+    rel = np.linalg.norm(diff) / max(np.linalg.norm(y_ref), 1e-300)
+    rms = np.sqrt(np.mean(y_ref ** 2))
+    mx = np.abs(diff).max() / max(rms, 1e-300)
+    assert rel <= Y_REL_L2, f"{what}: y relative L2 {rel:.3e} > {Y_REL_L2}"
+    assert mx <= MAXABS_RMS, f"{what}: y max abs error {mx:.3e} x RMS > {MAXABS_RMS}"
+    return rel, mx
 
 
 def output_errors(out_bits: np.ndarray, ref_out: np.ndarray):

@@ -6,8 +6,10 @@ import torch
 import oracle
 import workloads as W
 from fp8_routed_expert_gb300 import C, MoEError
-from harness import (DeviceWeights, check_output, check_routing, make_layer, reference, run,
-                     x_dev)
+from harness import (DeviceWeights, check_expert_y, check_output, check_routing, gpu_y,
+                     make_layer, oracle_expert_y, reference, reference_threaded, run,
+                     tile_class_experts, x_dev)
+from host_ref import combine_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -82,16 +84,29 @@ def test_tcgemv_ragged_batches(T):
     assert T < 300 or ref["counts"].max() > 16  # several tiles per expert
 
 
+def _check_all_positions(layer, ref, P, H, path):
+    """y of every position against the oracle's, expert by expert (every
+    tile of every active expert)."""
+    y = gpu_y(layer, P, H, path).cpu().numpy().astype(np.float64)
+    ref_y = ref["y"].reshape(P, H)[ref["perm"]]
+    off = ref["offsets"]
+    for e in np.nonzero(ref["counts"])[0]:
+        check_expert_y(y[off[e]:off[e + 1]], ref_y[off[e]:off[e + 1]],
+                       f"expert {e} ({off[e + 1] - off[e]} positions)")
+
+
 @pytest.mark.parametrize("T", [1, 16, 64])
 def test_wide_decode_tcgemv(T):
+    """Every token's output and every position's y (all tiles of all active
+    experts, 16-position tiles with ragged tails)."""
     fam, w, dw = weights("wide_decode")
     x = W.make_x(fam, T)
     layer = make_layer(fam, T)
     out, r = run(layer, x, dw, fam.top_k, "tcgemv")
-    tokens = None if T <= 16 else np.r_[0:4, T - 4:T]
-    ref = reference(x, w, fam.top_k, tokens=tokens)
+    ref = reference_threaded(x, w, fam.top_k)
     check_routing(r, ref, fam.n_experts)
-    check_output(out, ref, tokens)
+    check_output(out, ref)
+    _check_all_positions(layer, ref, T * fam.top_k, fam.hidden, "tcgemv")
 
 
 def test_intermediates_match_oracle():
@@ -141,15 +156,17 @@ def test_tensor_core_paths_y_match_oracle(T, path):
 
 @pytest.mark.parametrize("T", [512, 2048])
 def test_olmoe_prefill(T):
+    """Every token's output and every position's y: all 128-position tiles of
+    all 64 experts, full and ragged."""
     fam, w, dw = weights("olmoe_prefill")
     x = W.make_x(fam, T)
     layer = make_layer(fam, T)
     out, r = run(layer, x, dw, fam.top_k, "auto")
-    tokens = None if T <= 512 else np.r_[0:8, T // 2:T // 2 + 8, T - 8:T]
-    ref = reference(x, w, fam.top_k, tokens=tokens)
+    ref = reference_threaded(x, w, fam.top_k)
     check_routing(r, ref, fam.n_experts)
-    check_output(out, ref, tokens)
+    check_output(out, ref)
     assert (ref["counts"] > 0).all() and ref["counts"].max() > 2 * ref["counts"].mean()
+    _check_all_positions(layer, ref, T * fam.top_k, fam.hidden, layer.resolved_path(T))
 
 
 @pytest.mark.parametrize("T", [1, 16, 64])
@@ -158,27 +175,79 @@ def test_wide_decode(T):
     x = W.make_x(fam, T)
     layer = make_layer(fam, T)
     out, r = run(layer, x, dw, fam.top_k, "auto")
-    tokens = None if T <= 16 else np.r_[0:4, T - 4:T]
-    ref = reference(x, w, fam.top_k, tokens=tokens)
+    ref = reference_threaded(x, w, fam.top_k)
     check_routing(r, ref, fam.n_experts)
-    check_output(out, ref, tokens)
+    check_output(out, ref)
 
 
-def test_large_prefill_sampled():
+def test_large_prefill_whole_tiles():
+    """Large batch (T = 4096, E = 512, top-12, heavy imbalance): routing of
+    every token bit-exact; y of every position of the experts that cover the
+    tile classes (the busiest, one with count = 1 mod 128 or nearest, the
+    smallest, one in the middle and the last active expert); the output of 64
+    tokens spread over the batch and of every token of the busiest expert's
+    first 128-position tile."""
     fam, w, dw = weights("large_prefill")
-    T = 4096
+    T, k = 4096, fam.top_k
     x = W.make_x(fam, T)
     layer = make_layer(fam, T)
-    out, r = run(layer, x, dw, fam.top_k, "auto")
-    ref_r = reference(x, w, fam.top_k, tokens=[])
+    out, r = run(layer, x, dw, k, "auto")
+    ref_r = reference_threaded(x, w, k, tokens=[])
     check_routing(r, ref_r, fam.n_experts)
-    counts = ref_r["counts"]
+    counts, off, perm = ref_r["counts"], ref_r["offsets"], ref_r["perm"]
     assert (counts == 0).any(), "the workload should leave some experts without tokens"
+    P, H = T * k, fam.hidden
+    experts = tile_class_experts(counts, 128)
+    y_ref = oracle_expert_y(x, w, ref_r["idx"], experts)
+    y_dev = gpu_y(layer, P, H, layer.resolved_path(T))
+    for e in experts:
+        rows = y_dev[off[e]:off[e + 1]].cpu().numpy().astype(np.float64)
+        check_expert_y(rows, y_ref[e], f"expert {e} ({off[e + 1] - off[e]} positions)")
+    del y_dev
     busiest = int(np.argmax(counts))
-    t_busy = int(ref_r["perm"][ref_r["offsets"][busiest]] // fam.top_k)
-    tokens = np.array(sorted({0, 1, t_busy, T // 2, T - 1}))
-    ref = reference(x, w, fam.top_k, tokens=tokens)
+    tile_tokens = perm[off[busiest]:off[busiest] + 128] // k
+    tokens = np.unique(np.concatenate([np.linspace(0, T - 1, 64).astype(np.int64), tile_tokens]))
+    assert tokens.size >= 64 + 64
+    ref = reference_threaded(x, w, k, tokens=tokens)
     check_output(out, ref, tokens)
+
+
+@pytest.mark.parametrize("T,path", [(8, "tcgemv"), (8, "gemv"), (2048, "gemm")])
+def test_dense_ffn(T, path):
+    """A dense (or shared-expert) SwiGLU FFN in the same blockwise-FP8 format
+    (dragon.c, "Precision") is the layer with one expert and k = 1: every
+    token gets weight 1 and the permutation is the identity.  I = 8192 gives
+    64 column blocks of h per tile.  Every token's output and every
+    position's y are checked."""
+    fam, w, dw = weights("dense_ffn")
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, 1, path)
+    ref = reference_threaded(x, w, 1)
+    check_routing(r, ref, 1)
+    assert (r["wts"] == 1.0).all() and (r["perm"] == np.arange(T)).all()
+    check_output(out, ref)
+    _check_all_positions(layer, ref, T, fam.hidden, path)
+
+
+@pytest.mark.parametrize("T,path", [(300, "gemm"), (8, "tcgemv"), (64, "tcgemv"), (8, "gemv")])
+def test_combine_is_the_rank_order_fma_chain(T, path):
+    """The combine alone, bit for bit: out equals the host's f32 fma chain in
+    rank order over the GPU's own y and routing weights, rounded once to bf16
+    (the decode path's y is the f32 sum of its three term planes)."""
+    fam, w, dw = weights("olmoe_decode")
+    k = fam.top_k
+    x = W.make_x(fam, T)
+    layer = make_layer(fam, T)
+    out, r = run(layer, x, dw, k, path)
+    P, H = T * k, fam.hidden
+    if path == "tcgemv":
+        planes = layer.debug_buffer("y_terms", torch.float32, (3, P, H)).cpu().numpy()
+    else:
+        planes = layer.debug_buffer("y", torch.float32, (P, H)).cpu().numpy()[None]
+    acc = combine_f32(planes, r["inv"], r["wts"])
+    want = oracle.round_to_bf16(acc.astype(np.float64))
+    assert np.array_equal(out, want), f"{(out != want).sum()} of {out.size} outputs differ"
 
 
 # ------------------------------------------------------------------ degenerate cases

@@ -407,3 +407,23 @@ def test_planted_tie_break_mistake_fails(monkeypatch):
     monkeypatch.setattr(mo, "select_topk", _ties_high)
     res = mo.moe_forward(x, w.router_w, None, w.w13, w.s13, w.w2, w.s2, 3)
     assert not (res["idx"] == np.array([0, 1, 2])).all()
+
+
+# ----------------------------------------------------------------------------- threaded driver
+
+@pytest.mark.parametrize("name,T,tokens", [("tiny", 4, None), ("olmoe_prefill", 48, [0, 7, 47]),
+                                           ("olmoe_decode", 8, None)])
+def test_threaded_driver_is_the_oracle(name, T, tokens):
+    """oracle.threaded runs the oracle's own functions over tokens and expert
+    segments on a thread pool: every result equals moe_forward's exactly."""
+    from oracle import threaded
+    fam = W.family(name)
+    w = W.make_weights(fam)
+    x = W.make_x(fam, T)
+    a = oracle.moe_forward(x, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2, fam.top_k,
+                           tokens=tokens)
+    b = threaded.moe_forward(x, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2, fam.top_k,
+                             tokens=tokens, workers=3)
+    assert a.keys() == b.keys()
+    for key in a:
+        assert np.array_equal(a[key], b[key]), key
