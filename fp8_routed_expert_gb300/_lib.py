@@ -64,6 +64,7 @@ def lib():
                              ctypes.POINTER(ctypes.c_int64)], ctypes.c_int),
         "moe_kernel_name": ([ctypes.c_int], ctypes.c_char_p),
         "moe_launch_count": ([vp], ctypes.c_int64),
+        "moe_selftest_wait_timeout": ([vp, i64, vp, vp], ctypes.c_int),
         "moe_route_noalloc": ([vp, i64, i64, vp, vp, i64, i32, vp, vp, vp, vp, vp, vp, vp],
                               ctypes.c_int),
         "moe_debug_copy": ([vp, ctypes.c_char_p, vp, i64, ctypes.POINTER(ctypes.c_int64), vp],

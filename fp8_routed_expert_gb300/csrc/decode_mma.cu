@@ -181,16 +181,6 @@ __device__ __forceinline__ void st_global_f4_ordered(float *p, float4 v) {
                : "memory");
 }
 
-__device__ __forceinline__ int ld_acquire(const int32_t *p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 __device__ __forceinline__ void fail(volatile int *abort_flag, int *err) {
   *abort_flag = 1;
   set_error(err, DEV_ERR_TIMEOUT);
@@ -202,10 +192,7 @@ __device__ __forceinline__ bool wait_tile(const int32_t *done13, int64_t tile, i
                                           volatile int *abort_flag) {
   bool ok = true;
   if ((threadIdx.x & 31) == 0) {
-    const uint64_t t0 = global_timer_ns();
-    while (ld_acquire(done13 + tile) < need) {
-      if (*abort_flag || global_timer_ns() - t0 > DWAIT_NS) { ok = false; break; }
-    }
+    ok = wait_counter_ge(done13 + tile, need, abort_flag, DWAIT_NS);
     fence_proxy_async_global();
   }
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;

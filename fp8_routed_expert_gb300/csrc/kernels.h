@@ -143,4 +143,11 @@ cudaError_t launch_combine(const float *y, int n_planes, int64_t plane, const in
                            const float *wts, int64_t T, int k, int64_t H, __nv_bfloat16 *out,
                            cudaStream_t s);
 
+// One CTA whose waits (an mbarrier nothing arrives on, a global counter
+// nothing increments) run out after limit_ns each: records DEV_ERR_TIMEOUT in
+// *err and, if `which` is given, which waits gave up (bit 0 the mbarrier,
+// bit 1 the counter).  *idle_counter must be 0 and stay 0.
+cudaError_t launch_bounded_wait_selftest(const int32_t *idle_counter, uint64_t limit_ns, int *err,
+                                         int32_t *which, cudaStream_t s);
+
 }  // namespace fp8moe

@@ -45,6 +45,7 @@ struct moe_ctx {
   DecodeMaps dmaps;                              // tensor-core decode FFN operands
   float *xss = nullptr;                          // per-(token, 128 columns) sums of squares of x
   int32_t *done13 = nullptr;                     // decode FFN per-tile counters
+  int32_t *idle = nullptr;                       // a counter no kernel writes (bounded-wait self-test)
   const void *tm_w13_ptr = nullptr, *tm_w2_ptr = nullptr;  // weights the maps in .b describe
   const void *dmaps_w13 = nullptr, *dmaps_w2 = nullptr;    // weights dmaps describe
   int *err = nullptr;
@@ -360,6 +361,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->active, (size_t)E * 4},
       {(void **)&c->n_active, 16},
       {(void **)&c->ticket, 16},
+      {(void **)&c->idle, 16},
       {(void **)&c->done13, (size_t)((Pm + kDecodeTileN - 1) / kDecodeTileN + E + 1) * 4},
       {(void **)&c->xss, (size_t)(Tm * (H / 128)) * 4},
       {(void **)&c->xnorm, (size_t)Tm * 4},
@@ -487,6 +489,17 @@ int moe_status(moe_ctx *c) {
   if (flag & DEV_ERR_TIMEOUT) return MOE_ERR_DEVICE_TIMEOUT;
   if (flag & DEV_ERR_NONFINITE) return MOE_ERR_NONFINITE;
   if (flag) return MOE_ERR_DEVICE;
+  return MOE_OK;
+}
+
+int moe_selftest_wait_timeout(moe_ctx *c, int64_t limit_ns, int32_t *which, void *stream) {
+  if (c == nullptr || limit_ns <= 0 || limit_ns > 1000000000ll) return MOE_ERR_ARG;
+  if (which != nullptr && !aligned(which, 4)) return MOE_ERR_ALIGN;
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  c->n_launches += 1;
+  CUDA_TRY(launch_bounded_wait_selftest(c->idle, (uint64_t)limit_ns, c->err, which, s));
+  c->last_stream = s;
   return MOE_OK;
 }
 

@@ -68,6 +68,32 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// ------------------------------------------------------------------ global counters
+
+__device__ __forceinline__ int ld_acquire(const int32_t *p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Order this thread's generic-proxy view of global memory before its later
+// async-proxy (TMA) reads of it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until the global counter *p reaches `need` (acquire); false after
+// `limit_ns`, or when `abort` is given and *abort becomes non-zero.
+__device__ __forceinline__ bool wait_counter_ge(const int32_t *p, int need, volatile int *abort,
+                                                uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (ld_acquire(p) < need) {
+    if (abort != nullptr && *abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {

@@ -197,6 +197,25 @@ int moe_debug_copy(moe_ctx *ctx, const char *name, void *dst, int64_t capacity, 
                    void *stream);
 
 /*
+ * moe_selftest_wait_timeout - exercise the bounded device-side waits.  Every
+ * wait inside the layer's kernels (mbarriers of TMA copies and tensor-core
+ * work, cross-CTA counters) gives up after a time limit and records
+ * MOE_ERR_DEVICE_TIMEOUT instead of hanging the GPU.  This call enqueues one
+ * CTA that holds tensor memory as those kernels do and waits, with the same
+ * helpers, on an mbarrier that nothing arrives on and on a counter in the
+ * context's workspace that nothing increments, `limit_ns` each; both waits
+ * give up, the CTA frees its tensor memory and returns.
+ *   limit_ns : 1 .. 1e9 nanoseconds per wait.
+ *   which    : device int32 or NULL; receives the waits that gave up (bit 0
+ *              the mbarrier, bit 1 the counter: 3 when both did).
+ *   stream   : cudaStream_t or NULL.
+ * Afterwards moe_status reports MOE_ERR_DEVICE_TIMEOUT once (and clears it);
+ * the context stays usable.  No counterpart in the pages: it tests the
+ * failure handling of this library.
+ */
+int moe_selftest_wait_timeout(moe_ctx *ctx, int64_t limit_ns, int32_t *which, void *stream);
+
+/*
  * moe_route_noalloc - the routing step alone (steps 1 and 2 above) for callers
  * that may not allocate device memory once running: applications that hand
  * all device memory to their own allocator at start-up, or inference loops

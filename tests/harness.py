@@ -8,7 +8,13 @@ Tolerances (the CUDA path against the f64 oracle):
     bound (about 1e-5 relative to ||x|| ||W_e|| at the largest H here) and a
     few f32 roundings of the softmax; typical errors are about 1e-7;
   * bf16 outputs: relative L2 error <= 1e-2 and max |error| <= 2e-2 x RMS of
-    the oracle output, both against the unrounded f64 oracle.
+    the oracle output, both against the unrounded f64 oracle.  The max-abs
+    bound counts the error beyond the output format's own rounding: an
+    element may also be off by half a bf16 ulp of its exact value.  Rounding
+    the exact layer once to bf16 already reaches 2.40e-2 x RMS on the large
+    prefill batch (outputs up to 7.4 x RMS, where half an ulp is up to
+    1/512 of the value), so the bound read literally would reject even the
+    correctly rounded output.
 """
 from __future__ import annotations
 
@@ -121,13 +127,25 @@ def check_expert_y(y_gpu_rows: np.ndarray, y_ref: np.ndarray, what: str = ""):
     return rel, mx
 
 
+def bf16_half_ulp(v: np.ndarray) -> np.ndarray:
+    """Half the spacing of bf16 values at |v| (8 significant bits: the spacing
+    in [2^e, 2^(e+1)) is 2^(e-7); 2^-133 below 2^-126)."""
+    _, ex = np.frexp(np.abs(v))      # |v| in [2^(ex-1), 2^ex)
+    e = np.maximum(ex - 1, -126)
+    return np.ldexp(0.5, e - 7)
+
+
 def output_errors(out_bits: np.ndarray, ref_out: np.ndarray):
+    """(relative L2 error, max |error| beyond half a bf16 ulp / RMS, max
+    |error| / RMS) of bf16 outputs against the exact f64 values."""
     got = oracle.bf16_to_f64(out_bits)
     diff = got - ref_out
     rms = np.sqrt(np.mean(ref_out ** 2))
     rel = np.linalg.norm(diff) / max(np.linalg.norm(ref_out), 1e-300)
-    mx = np.abs(diff).max() / max(rms, 1e-300) if diff.size else 0.0
-    return rel, mx
+    if not diff.size:
+        return rel, 0.0, 0.0
+    excess = np.maximum(np.abs(diff) - bf16_half_ulp(ref_out), 0.0)
+    return rel, excess.max() / max(rms, 1e-300), np.abs(diff).max() / max(rms, 1e-300)
 
 
 def check_routing(r: dict, ref: dict, n_experts: int):
@@ -143,7 +161,8 @@ def check_routing(r: dict, ref: dict, n_experts: int):
 
 def check_output(out_bits: np.ndarray, ref: dict, tokens=None):
     sel = ref["tokens"] if tokens is None else tokens
-    rel, mx = output_errors(out_bits[sel], ref["out"])
+    rel, mx, mx_total = output_errors(out_bits[sel], ref["out"])
     assert rel <= REL_L2, f"relative L2 error {rel:.3e} > {REL_L2}"
-    assert mx <= MAXABS_RMS, f"max abs error {mx:.3e} x RMS > {MAXABS_RMS}"
+    assert mx <= MAXABS_RMS, (f"max abs error beyond the bf16 rounding {mx:.3e} x RMS > "
+                              f"{MAXABS_RMS} (total {mx_total:.3e} x RMS)")
     return rel, mx

@@ -55,6 +55,7 @@ def test_null_arguments(L):
     assert L.moe_status(None) == moe.C["MOE_ERR_ARG"]
     assert L.moe_set_path(None, 0) == moe.C["MOE_ERR_ARG"]
     assert L.moe_resolve_path(None, 1) == moe.C["MOE_ERR_ARG"]
+    assert L.moe_selftest_wait_timeout(None, 1000, None, None) == moe.C["MOE_ERR_ARG"]
 
 
 def test_error_strings(L):

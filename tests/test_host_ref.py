@@ -48,3 +48,16 @@ def test_combine_chain_order():
     w = np.array([[0.25, 0.75], [0.5, 0.5]], dtype=np.float32)
     acc = combine_f32(y, inv, w)
     assert acc.tolist() == [[0.25 * 5 + 0.75 * 1, 0.25 * 6 + 0.75 * 2], [0.5 * 3 + 0.5 * 7, 0.5 * 4 + 0.5 * 8]]
+
+
+def test_bf16_half_ulp_bounds_the_correct_rounding():
+    import oracle
+    from harness import bf16_half_ulp
+    rng = np.random.default_rng(5)
+    v = rng.standard_normal(20000) * 2.0 ** rng.integers(-20, 20, 20000)
+    r = oracle.bf16_to_f64(oracle.round_to_bf16(v))
+    assert (np.abs(r - v) <= bf16_half_ulp(v)).all()
+    # at a midpoint the bound is attained: 1 + 2^-8 lies halfway between
+    # the bf16 values 1 and 1 + 2^-7
+    assert bf16_half_ulp(np.array([1.0 + 2.0 ** -8]))[0] == 2.0 ** -8
+    assert bf16_half_ulp(np.array([-3.0]))[0] == 2.0 ** -7
