@@ -85,11 +85,18 @@ bool encode_u8_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t row
 cudaError_t launch_act_quant(const __nv_bfloat16 *x, const int32_t *perm, int64_t P, int k,
                              int64_t H, int64_t Pmax, uint8_t *a_hi, uint8_t *a_lo, float *a_scale,
                              int sms, cudaStream_t s);
-// Tensor maps of one grouped GEMM: up to three activation terms and the weights.
+// Tensor maps of one grouped GEMM: up to three activation terms and the
+// weights (loads), and the output boxes (stores): the three e4m3 terms of h
+// (gate/up GEMM: boxes of 32 rows x 64 bytes) or y (down GEMM, st[0]: f32,
+// boxes of 32 rows x 32 columns, 128-byte swizzle).
 struct TmapSet {
   CUtensorMap a[3];
   CUtensorMap b;
+  CUtensorMap st[3];
 };
+// Store maps of the grouped GEMM outputs (see TmapSet).
+bool encode_h_store_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows);
+bool encode_y_store_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows);
 // mode 1: gate/up + SwiGLU -> three-term e4m3 h (two activation terms in);
 // mode 2: down -> f32 y (three activation terms in).
 cudaError_t launch_grouped_gemm(int mode, const TmapSet &tm, const int32_t *offsets,

@@ -55,11 +55,15 @@ constexpr int THREADS = 64 + 32 * NUM_EPI_WARPS;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s per wait
 
+// Output staging per epilogue warp: the boxes its 32 rows send to global
+// memory by TMA store (gate/up: 3 h terms x 32 rows x 32 bytes per round;
+// down: two 32 x 32 f32 boxes).
 template <int NT>
 struct Pipe {
   static constexpr int STAGE_BYTES = NT * A_TILE + B_TILE;  // 64 KiB (NT=2) or 80 KiB (NT=3)
   static constexpr int STAGES = NT == 2 ? 3 : 2;
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024;
+  static constexpr int STG_WARP = NT == 2 ? 4096 : 8192;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + (size_t)NUM_EPI_WARPS * STG_WARP + 1024;
 };
 
 struct GemmArgs {
@@ -132,6 +136,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
     fence_mbar_init();
     for (int t = 0; t < NT; ++t) prefetch_tmap(&tm.a[t]);
     prefetch_tmap(&tm.b);
+    for (int t = 0; t < (MODE == 1 ? 3 : 1); ++t) prefetch_tmap(&tm.st[t]);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, TMEM_COLS);
@@ -214,39 +219,38 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
     // ---------------------------------------------------------------- promotion + epilogue
     const int quarter = warp & 3;             // TMEM lanes this warp may read
     const int half = (warp - 2) >> 2;         // column half of the 256-wide tile
+    uint8_t *stg_warp = smem + (size_t)STAGES * STAGE_BYTES + (size_t)(warp - 2) * Pipe<NT>::STG_WARP;
     const int r_in_tile = quarter * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     int buf = 0;
     uint32_t bphase = 0;
     const int64_t wrow_blocks = (MODE == 1) ? 2 * p.I / 128 : p.H / 128;
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
-      const ItemCoords c = item_coords(p, item);
+      ItemCoords c = item_coords(p, item);
       const int64_t row = c.m0 + r_in_tile;
-      const bool valid = row < c.row_end;
+      // weight scales of the two 128-row blocks of this tile half: gate and up
+      // rows (GEMM1) or one W2 row block (GEMM2), one per K block
       const float *ws = p.w_scale + (int64_t)c.e * wrow_blocks * nkb;
-      int64_t blk0, blk1;
-      if (MODE == 1) {
-        blk0 = c.nb;                 // gate rows of this column block
-        blk1 = p.I / 128 + c.nb;     // up rows
-      } else {
-        blk0 = blk1 = 2 * (int64_t)c.nb + half;
-      }
+      const float *ws0 = ws + (MODE == 1 ? (int64_t)c.nb : 2 * (int64_t)c.nb + half) * nkb;
+      const float *ws1 = ws + (MODE == 1 ? p.I / 128 + c.nb : 2 * (int64_t)c.nb + half) * nkb;
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.f;
       bool ok = true;
-      const float *sa_p = p.a_scale + (row < p.Pmax ? row : 0);
       const bool sa_ok = row < p.Pmax;
+      const float *sa_p = p.a_scale + (sa_ok ? row : 0);
       // the scales of K block kb + 1 are loaded while block kb is promoted,
       // so their latency is not on the path between the MMA and the epilogue
       float sa_n = sa_ok ? __ldg(sa_p) : 0.f;
-      float s0_n = __ldg(ws + blk0 * nkb), s1_n = __ldg(ws + blk1 * nkb);
-      for (int64_t kb = 0; kb < nkb; ++kb) {
+      float s0_n = __ldg(ws0), s1_n = __ldg(ws1);
+      const int nkb32 = (int)nkb;
+      for (int kb = 0; kb < nkb32; ++kb) {
         const float c0 = sa_n * s0_n, c1 = sa_n * s1_n;
-        if (kb + 1 < nkb) {
-          sa_n = sa_ok ? __ldg(sa_p + (kb + 1) * p.Pmax) : 0.f;
-          s0_n = __ldg(ws + blk0 * nkb + kb + 1);
-          s1_n = __ldg(ws + blk1 * nkb + kb + 1);
+        if (kb + 1 < nkb32) {
+          sa_p += p.Pmax;
+          sa_n = sa_ok ? __ldg(sa_p) : 0.f;
+          s0_n = __ldg(ws0 + kb + 1);
+          s1_n = __ldg(ws1 + kb + 1);
         }
         // no early exit on the abort flag here: the epilogue warps share a
         // named barrier, so they must all stop at the same (timed-out) wait
@@ -257,12 +261,12 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
         }
         tc_fence_after();
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          float v[32];
-          tmem_ld_32x32b_x32(t_lane + (uint32_t)(buf * BN + half * 128 + ch * 32), v);
-          const float sc = ch < 2 ? c0 : c1;
+        for (int ch = 0; ch < 8; ++ch) {
+          float v[16];
+          tmem_ld_32x32b_x16(t_lane + (uint32_t)(buf * BN + half * 128 + ch * 16), v);
+          const float sc = ch < 4 ? c0 : c1;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) acc[ch * 32 + j] = fmaf(v[j], sc, acc[ch * 32 + j]);
+          for (int j = 0; j < 16; ++j) acc[ch * 16 + j] = fmaf(v[j], sc, acc[ch * 16 + j]);
         }
         tc_fence_before();
         __syncwarp();
@@ -271,6 +275,10 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
         if (buf == 0) bphase ^= 1u;
       }
       if (!ok) break;
+      // the item's coordinates again, rather than keeping them in registers
+      // through the K loop
+      c = item_coords(p, item);
+      const bool valid = row < c.row_end;
 
       if (MODE == 1) {
         float amax = 0.f;
@@ -283,37 +291,114 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
         named_bar_sync(1, 32 * NUM_EPI_WARPS);
         const float am = fmaxf(amax_x[0][r_in_tile], amax_x[1][r_in_tile]);
         named_bar_sync(1, 32 * NUM_EPI_WARPS);
-        if (valid) {
-          const int ex = e4m3_block_exponent(am);
-          const Pow2 down = pow2_factors(-ex);
-          const int64_t off = row * p.I + (int64_t)c.nb * 128 + half * 64;
+        // The warp's 32 rows go out through its staging buffer: whole boxes
+        // by TMA store (asynchronous) when all 32 rows lie in the segment,
+        // else the valid rows by plain 16-byte copies from the buffer.
+        const int ex = e4m3_block_exponent(am);
+        const Pow2 down = pow2_factors(-ex);
+        const int32_t x0 = (int32_t)(c.nb * 128 + half * 64), y0 = (int32_t)(c.m0 + quarter * 32);
+        const int64_t nrows = c.row_end - y0;  // rows of this warp in the segment (may be <= 0)
+        const bool full_q = nrows >= 32;       // warp-uniform
+        uint32_t ln;  // opaque copy of the lane index (see the down GEMM's tail)
+        asm volatile("mov.u32 %0, %1;" : "=r"(ln) : "r"((uint32_t)lane));
+        uint8_t *srow = stg_warp + ln * 32;
 #pragma unroll
-          for (int j = 0; j < 64; j += 16) {
+        for (int rd = 0; rd < 2; ++rd) {
+          if (lane == 0) bulk_wait_read<0>();  // earlier boxes have left the buffer
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 32; j += 16) {
             uint32_t w0[4], w1[4], w2[4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               uint32_t a[3], b[3];
-              e4m3_terms<3>(down(acc[j + 4 * m]), down(acc[j + 4 * m + 1]), a);
-              e4m3_terms<3>(down(acc[j + 4 * m + 2]), down(acc[j + 4 * m + 3]), b);
+              const int v = rd * 32 + j + 4 * m;
+              e4m3_terms<3>(down(acc[v]), down(acc[v + 1]), a);
+              e4m3_terms<3>(down(acc[v + 2]), down(acc[v + 3]), b);
               w0[m] = a[0] | (b[0] << 16);
               w1[m] = a[1] | (b[1] << 16);
               w2[m] = a[2] | (b[2] << 16);
             }
-            *reinterpret_cast<uint4 *>(p.h_t0 + off + j) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
-            *reinterpret_cast<uint4 *>(p.h_t1 + off + j) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
-            *reinterpret_cast<uint4 *>(p.h_t2 + off + j) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+            *reinterpret_cast<uint4 *>(srow + 0 * 1024 + j) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
+            *reinterpret_cast<uint4 *>(srow + 1 * 1024 + j) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+            *reinterpret_cast<uint4 *>(srow + 2 * 1024 + j) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
           }
-          if (half == 0) p.h_scale[(int64_t)c.nb * p.Pmax + row] = ldexpf(1.f, ex);
-        }
-      } else {
-        if (valid) {
-          float4 *dy = reinterpret_cast<float4 *>(p.y + row * p.H + (int64_t)c.nb * 256 + half * 128);
+          if (full_q) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm.st[0], stg_warp, x0 + rd * 32, y0);
+              tma_store_2d(&tm.st[1], stg_warp + 1024, x0 + rd * 32, y0);
+              tma_store_2d(&tm.st[2], stg_warp + 2048, x0 + rd * 32, y0);
+              bulk_commit();
+            }
+          } else if (nrows > 0) {
+            __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            dy[j] = make_float4(acc[4 * j], acc[4 * j + 1], acc[4 * j + 2], acc[4 * j + 3]);
+            for (int i = 0; i < 6; ++i) {  // 3 terms x 32 rows x two 16-byte pieces
+              const int idx = i * 32 + lane, t = idx >> 6, r = (idx >> 1) & 31, pc = idx & 1;
+              if (r < nrows) {
+                uint8_t *dst = (t == 0 ? p.h_t0 : t == 1 ? p.h_t1 : p.h_t2) +
+                               (int64_t)(y0 + r) * p.I + x0 + rd * 32 + pc * 16;
+                *reinterpret_cast<uint4 *>(dst) =
+                    *reinterpret_cast<const uint4 *>(stg_warp + t * 1024 + r * 32 + pc * 16);
+              }
+            }
+            __syncwarp();
+          }
+        }
+        if (valid && half == 0) p.h_scale[(int64_t)c.nb * p.Pmax + row] = ldexpf(1.f, ex);
+      } else {
+        // four 32 x 32 f32 boxes through two 128-byte-swizzled buffers (16-byte
+        // piece q of row r sits at piece q ^ (r % 8)): TMA stores when all 32
+        // rows of the warp lie in the segment, else plain copies of the valid rows
+        const int32_t y0 = (int32_t)(c.m0 + quarter * 32);
+        const int64_t nrows = c.row_end - y0;
+        const bool full_q = nrows >= 32;  // warp-uniform
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint8_t *b = stg_warp + (ch & 1) * 4096;
+          const int32_t x = (int32_t)(c.nb * 256 + half * 128 + ch * 32);
+          if (ch >= 2) {
+            if (lane == 0) bulk_wait_read<1>();  // the box of chunk ch - 2 has left b
+            __syncwarp();
+          }
+          // the row's base address is formed here (an opaque copy of the lane
+          // index), so the compiler does not keep eight swizzled addresses
+          // live through the K loop
+          uint32_t ln;
+          asm volatile("mov.u32 %0, %1;" : "=r"(ln) : "r"((uint32_t)lane));
+          uint8_t *brow = b + ln * 128;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4 *>(brow + ((q ^ (ln & 7)) << 4)) =
+                make_float4(acc[ch * 32 + 4 * q], acc[ch * 32 + 4 * q + 1], acc[ch * 32 + 4 * q + 2],
+                            acc[ch * 32 + 4 * q + 3]);
+          if (full_q) {
+            fence_proxy_async_shared();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tm.st[0], b, x, y0);
+              bulk_commit();
+            }
+          } else if (nrows > 0) {
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {  // 32 rows x eight 16-byte pieces
+              const int idx = i * 32 + lane, r = idx >> 3, q = idx & 7;
+              if (r < nrows)
+                *reinterpret_cast<float4 *>(p.y + (int64_t)(y0 + r) * p.H + x + q * 4) =
+                    *reinterpret_cast<const float4 *>(b + r * 128 + ((q ^ (r & 7)) << 4));
+            }
+            __syncwarp();
+          }
         }
       }
     }
+    if (lane == 0) bulk_wait<0>();  // every TMA store of this warp has completed
+    __syncwarp();
   }
 
   __syncthreads();
@@ -446,6 +531,30 @@ bool encode_u8_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t row
                   estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool encode_h_store_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_y_store_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 cudaError_t launch_act_quant(const __nv_bfloat16 *x, const int32_t *perm, int64_t P, int k,

@@ -22,6 +22,13 @@
  *   code  = e4m3_rne(clamp(v / scale, -448, 448)).
  * This is the weight format the dragon.c page states under "Precision"
  * (e4m3 with 128x128 blockwise f32 scales).
+ *
+ * The FP4 expert format (NVFP4, the Qwen post's experts) is generated from
+ * the same normal streams: per expert matrix a global f32 scale
+ * g = absmax / (6 * 448) (1 if all zero); per 16 consecutive values of a row
+ * an e4m3 block scale s = e4m3_rne(block absmax / (6 g)); codes
+ * e2m1_rne(clamp(v / (s g), -6, 6)) (0 where s is 0), two per byte, the
+ * even element in the low nibble.
  */
 #include <math.h>
 #include <pthread.h>
@@ -92,10 +99,33 @@ void gen_e4m3_encode_array(const float *in, int64_t n, uint8_t *out) {
   for (int64_t i = 0; i < n; ++i) out[i] = gen_e4m3_encode(in[i]);
 }
 
+/* e4m3 ("fn") code -> value (finite codes only). */
+static double e4m3_decode(uint8_t c) {
+  int e = (c >> 3) & 0xF, m = c & 7;
+  double v = e == 0 ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+  return (c & 0x80) ? -v : v;
+}
+
+/* f32 -> e2m1 code (sign bit 3; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are
+ * codes 0..7), round to nearest with ties to the even code, saturating at
+ * +-6. */
+uint8_t gen_e2m1_encode(float y) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  const uint8_t sign = signbit(y) ? 0x8 : 0x0;
+  const double a = fabs((double)y);
+  if (a >= 6.0) return sign | 7;
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const double d = fabs(a - mag[c]), db = fabs(a - mag[best]);
+    if (d < db || (d == db && (c & 1) == 0)) best = c;
+  }
+  return sign | (uint8_t)best;
+}
+
 /* ---------------------------------------------------------------- threads */
 
 typedef struct {
-  int kind; /* 0 = f32, 1 = bf16, 2 = blockwise e4m3 */
+  int kind; /* 0 = f32, 1 = bf16, 2 = blockwise e4m3, 3 = nvfp4 (one expert per unit) */
   uint64_t key;
   int64_t lo, hi; /* work range: elements (kinds 0, 1) or blocks (kind 2) */
   double std;
@@ -105,6 +135,9 @@ typedef struct {
   int64_t R, C;
   uint8_t *codes;
   float *scales;
+  /* nvfp4 */
+  uint8_t *bscales;
+  float *gscales;
 } job_t;
 
 static void run_flat(job_t *j) {
@@ -153,9 +186,51 @@ static void run_blocks(job_t *j) {
   free(buf);
 }
 
+/* Experts [lo, hi) of an nvfp4 matrix set; element (e, r, c) is normal
+ * number (e*R + r)*C + c of the stream, as in run_blocks. */
+static void run_nvfp4(job_t *j) {
+  const int64_t R = j->R, C = j->C;
+  for (int64_t e = j->lo; e < j->hi; ++e) {
+    const uint64_t base = (uint64_t)(e * R * C); /* even: C is a multiple of 16 */
+    float amax = 0.0f;
+    for (uint64_t i = 0; i < (uint64_t)(R * C); i += 2) {
+      double z0, z1;
+      normal_pair(j->key, (base + i) >> 1, &z0, &z1);
+      const float a0 = fabsf((float)(j->std * z0)), a1 = fabsf((float)(j->std * z1));
+      if (a0 > amax) amax = a0;
+      if (a1 > amax) amax = a1;
+    }
+    const float g = amax > 0.0f ? amax / (6.0f * 448.0f) : 1.0f;
+    j->gscales[e] = g;
+    for (int64_t r = 0; r < R; ++r) {
+      for (int64_t c0 = 0; c0 < C; c0 += 16) {
+        float v[16], bmax = 0.0f;
+        for (int c = 0; c < 16; c += 2) {
+          double z0, z1;
+          normal_pair(j->key, (base + (uint64_t)(r * C + c0 + c)) >> 1, &z0, &z1);
+          v[c] = (float)(j->std * z0);
+          v[c + 1] = (float)(j->std * z1);
+        }
+        for (int c = 0; c < 16; ++c)
+          if (fabsf(v[c]) > bmax) bmax = fabsf(v[c]);
+        const uint8_t sc = gen_e4m3_encode(bmax / (6.0f * g));
+        j->bscales[(e * R + r) * (C / 16) + c0 / 16] = sc;
+        const double sv = e4m3_decode(sc) * (double)g;
+        uint8_t *dst = j->codes + (e * R + r) * (C / 2) + c0 / 2;
+        for (int c = 0; c < 16; c += 2) {
+          const uint8_t q0 = sv > 0.0 ? gen_e2m1_encode((float)(v[c] / sv)) : 0;
+          const uint8_t q1 = sv > 0.0 ? gen_e2m1_encode((float)(v[c + 1] / sv)) : 0;
+          dst[c / 2] = (uint8_t)(q0 | (q1 << 4));
+        }
+      }
+    }
+  }
+}
+
 static void *thread_main(void *arg) {
   job_t *j = (job_t *)arg;
-  if (j->kind == 2) run_blocks(j);
+  if (j->kind == 3) run_nvfp4(j);
+  else if (j->kind == 2) run_blocks(j);
   else run_flat(j);
   return NULL;
 }
@@ -218,4 +293,23 @@ int gen_blockwise_e4m3(uint64_t seed, uint64_t tensor_id, int64_t E, int64_t R, 
   p.codes = codes;
   p.scales = scales;
   return run_parallel(p, E * (R / 128) * (C / 128), nthreads);
+}
+
+/* E matrices of R x C values f32(std * z) in the FP4 expert format:
+ * codes [E,R,C/2] u8 (two e2m1 per byte, even element low), block scales
+ * [E,R,C/16] e4m3 codes, global scales [E] f32.  C % 16 == 0. */
+int gen_nvfp4(uint64_t seed, uint64_t tensor_id, int64_t E, int64_t R, int64_t C, double std,
+              uint8_t *codes, uint8_t *bscales, float *gscales, int nthreads) {
+  if (C % 16 != 0 || R <= 0 || E < 0) return -1;
+  job_t p;
+  memset(&p, 0, sizeof p);
+  p.kind = 3;
+  p.key = gen_stream_key(seed, tensor_id);
+  p.std = std;
+  p.R = R;
+  p.C = C;
+  p.codes = codes;
+  p.bscales = bscales;
+  p.gscales = gscales;
+  return run_parallel(p, E, nthreads);
 }
