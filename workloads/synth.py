@@ -47,7 +47,10 @@ def lib():
         L.gen_normal_f32.argtypes = [u64, u64, i64, dbl, vp, i32]
         L.gen_normal_bf16.argtypes = [u64, u64, i64, dbl, vp, i32]
         L.gen_blockwise_e4m3.argtypes = [u64, u64, i64, i64, i64, dbl, vp, vp, i32]
-        for f in (L.gen_normal_f32, L.gen_normal_bf16, L.gen_blockwise_e4m3):
+        L.gen_nvfp4.argtypes = [u64, u64, i64, i64, i64, dbl, vp, vp, vp, i32]
+        L.gen_e2m1_encode.argtypes = [ctypes.c_float]
+        L.gen_e2m1_encode.restype = ctypes.c_uint8
+        for f in (L.gen_normal_f32, L.gen_normal_bf16, L.gen_blockwise_e4m3, L.gen_nvfp4):
             f.restype = i32
         _lib = L
     return _lib
@@ -78,6 +81,20 @@ def blockwise_e4m3(seed: int, tid: int, E: int, R: int, C: int, std: float, nthr
     if rc != 0:
         raise ValueError("R and C must be multiples of 128")
     return codes, scales
+
+
+def nvfp4(seed: int, tid: int, E: int, R: int, C: int, std: float, nthreads=None):
+    """E matrices R x C of N(0, std) values in the FP4 expert format: packed
+    e2m1 codes [E, R, C/2], e4m3 block scales [E, R, C/16], f32 global
+    scales [E] (the same normal streams as ``blockwise_e4m3``)."""
+    codes = np.empty((E, R, C // 2), dtype=np.uint8)
+    bsc = np.empty((E, R, C // 16), dtype=np.uint8)
+    gsc = np.empty((E,), dtype=np.float32)
+    rc = lib().gen_nvfp4(seed, tid, E, R, C, std, codes.ctypes.data, bsc.ctypes.data,
+                         gsc.ctypes.data, _threads(nthreads))
+    if rc != 0:
+        raise ValueError("C must be a multiple of 16")
+    return codes, bsc, gsc
 
 
 def e4m3_encode(values: np.ndarray) -> np.ndarray:
@@ -111,6 +128,31 @@ def make_weights(fam: Family, nthreads=None) -> LayerWeights:
     w13, s13 = blockwise_e4m3(s, TID_W13, E, 2 * I, H, fam.w_std, nthreads)
     w2, s2 = blockwise_e4m3(s, TID_W2, E, H, I, fam.w_std, nthreads)
     return LayerWeights(router_w, bias, w13, s13, w2, s2)
+
+
+@dataclass
+class LayerWeightsFP4:
+    router_w: np.ndarray            # f32 [E, H]
+    router_bias: np.ndarray | None  # f32 [E] or None
+    w13: np.ndarray                 # u8 [E, 2I, H/2] packed e2m1; rows [0,I) gate, [I,2I) up
+    sf13: np.ndarray                # u8 e4m3 [E, 2I, H/16]
+    g13: np.ndarray                 # f32 [E]
+    w2: np.ndarray                  # u8 [E, H, I/2]
+    sf2: np.ndarray                 # u8 e4m3 [E, H, I/16]
+    g2: np.ndarray                  # f32 [E]
+
+
+def make_weights_fp4(fam: Family, nthreads=None) -> LayerWeightsFP4:
+    """The family's layer with FP4 experts: the same router and the same
+    normal streams as ``make_weights``, quantised to the FP4 format."""
+    E, H, I, s = fam.n_experts, fam.hidden, fam.inter, fam.seed
+    router_w = normal_f32(s, TID_ROUTER_W, (E, H), fam.router_std, nthreads)
+    bias = None
+    if fam.bias_std is not None:
+        bias = normal_f32(s, TID_ROUTER_BIAS, (E,), fam.bias_std, nthreads)
+    w13, sf13, g13 = nvfp4(s, TID_W13, E, 2 * I, H, fam.w_std, nthreads)
+    w2, sf2, g2 = nvfp4(s, TID_W2, E, H, I, fam.w_std, nthreads)
+    return LayerWeightsFP4(router_w, bias, w13, sf13, g13, w2, sf2, g2)
 
 
 def make_x(fam: Family, T: int, nthreads=None) -> np.ndarray:
