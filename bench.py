@@ -68,6 +68,9 @@ def parse():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "gemv", "gemm", "tcgemv"],
                     help="force one of the layer's expert paths (default: the library's choice)")
+    ap.add_argument("--format", default="fp8", choices=["fp8", "nvfp4"],
+                    help="expert weight format: blockwise e4m3 (default) or NVFP4 (e2m1 + e4m3 "
+                         "scale per 16 weights + f32 global per expert matrix)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -102,13 +105,19 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def selected_bytes(fam, counts) -> dict:
+def selected_bytes(fam, counts, fmt: str = "fp8") -> dict:
     """Algorithmic bytes of one step: every active expert's codes and scales
-    once, the router, the activations in and out."""
+    once, the router, the activations in and out.  fp8: e4m3 codes + one f32
+    per 128x128 block; nvfp4: half a byte per weight + one e4m3 per 16
+    weights + one f32 per matrix."""
     H, I, E = fam.hidden, fam.inter, fam.n_experts
     n_act = int((np.asarray(counts) > 0).sum())
-    w13 = 2 * I * H + 4 * (2 * I // 128) * (H // 128)
-    w2 = H * I + 4 * (H // 128) * (I // 128)
+    if fmt == "nvfp4":
+        w13 = 2 * I * H // 2 + 2 * I * H // 16 + 4
+        w2 = H * I // 2 + H * I // 16 + 4
+    else:
+        w13 = 2 * I * H + 4 * (2 * I // 128) * (H // 128)
+        w2 = H * I + 4 * (H // 128) * (I // 128)
     return dict(n_active=n_act, w13=n_act * w13, w2=n_act * w2, router=E * H * 4)
 
 
@@ -190,10 +199,16 @@ import workloads as W
 from oracle import threaded
 fam, T = W.parse_workload(sys.argv[2])
 budget, n, reps_max, warm = float(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5]), int(sys.argv[6])
-w = W.make_weights(fam)
 x = W.make_x(fam, T)[:n]
-run = lambda: threaded.moe_forward(x, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2,
-                                   fam.top_k)
+if sys.argv[7] == "nvfp4":
+    from oracle import nvfp4
+    w = W.make_weights_fp4(fam)
+    run = lambda: nvfp4.moe_forward_nvfp4(x, w.router_w, w.router_bias, w.w13, w.sf13, w.g13,
+                                          w.w2, w.sf2, w.g2, fam.top_k)
+else:
+    w = W.make_weights(fam)
+    run = lambda: threaded.moe_forward(x, w.router_w, w.router_bias, w.w13, w.s13, w.w2, w.s2,
+                                       fam.top_k)
 for _ in range(warm):
     run()
 times = []
@@ -202,37 +217,40 @@ while True:
     a = time.perf_counter(); run(); times.append(time.perf_counter() - a)
     if len(times) >= reps_max or (budget > 0 and time.perf_counter() - t0 >= budget):
         break
-print(json.dumps({"times": times, "n": n, "T": T, "cores": threaded.default_workers()}))
+print(json.dumps({"times": times, "n": n, "T": T,
+                  "cores": 1 if sys.argv[7] == "nvfp4" else threaded.default_workers()}))
 """
 
 
-def _oracle_child(workload: str, budget: float, reps_max: int, warm: int) -> dict:
+def _oracle_child(workload: str, budget: float, reps_max: int, warm: int, fmt: str = "fp8") -> dict:
     fam, T = W.parse_workload(workload)
     n = oracle_sample_tokens(fam, T)
     # one expert per thread, each with a single-threaded BLAS
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     r = subprocess.run([sys.executable, "-c", _ORACLE_CHILD, ROOT, workload, str(budget), str(n),
-                        str(reps_max), str(warm)], capture_output=True, text=True, env=env,
+                        str(reps_max), str(warm), fmt], capture_output=True, text=True, env=env,
                        timeout=3600)
     if r.returncode != 0:
         raise RuntimeError("oracle run failed: " + r.stderr[-2000:])
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def _oracle_sample_text(workload: str, d: dict) -> str:
+def _oracle_sample_text(workload: str, d: dict, fmt: str = "fp8") -> str:
+    how = ("FP4 f64 oracle, one thread" if fmt == "nvfp4" else
+           f"f64 oracle threaded over tokens (router) and expert segments (FFN) on "
+           f"{d['cores']} host threads")
     return (f"whole layer (routing, experts, combine) on the first {d['n']} of the "
-            f"{d['T']} tokens of {workload}, f64 oracle threaded over tokens (router) and "
-            f"expert segments (FFN) on {d['cores']} host threads; every expert the sample "
-            f"touches is dequantised once per pass")
+            f"{d['T']} tokens of {workload}, {how}; every expert the sample touches is "
+            f"dequantised once per pass")
 
 
-def oracle_rate(workload: str, seconds: float) -> dict:
-    """Oracle tokens/s on all host cores: passes over the bounded sample for
+def oracle_rate(workload: str, seconds: float, fmt: str = "fp8") -> dict:
+    """Oracle tokens/s on the host cores: passes over the bounded sample for
     about `seconds`, in a fresh process."""
-    d = _oracle_child(workload, seconds, 1000, 0)
+    d = _oracle_child(workload, seconds, 1000, 0, fmt)
     el = sum(d["times"])
     return dict(value=len(d["times"]) * d["n"] / el, unit=UNIT, cores=d["cores"], kind="oracle",
-                sample=f"{len(d['times'])} passes, {el:.1f} s: " + _oracle_sample_text(workload, d),
+                sample=f"{len(d['times'])} passes, {el:.1f} s: " + _oracle_sample_text(workload, d, fmt),
                 seconds=el)
 
 
@@ -336,13 +354,17 @@ def run_native(args, rank, local_rank, world):
 
     fam, T = W.parse_workload(args.workload)
     k = fam.top_k
+    fp4 = args.format == "nvfp4"
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = W.make_weights(fam)
+    w = W.make_weights_fp4(fam) if fp4 else W.make_weights(fam)
     xb = W.make_x(fam, T)
     g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     rw, rb = g(w.router_w), (None if w.router_bias is None else g(w.router_bias))
-    w13, s13, w2, s2 = g(w.w13), g(w.s13), g(w.w2), g(w.s2)
+    if fp4:
+        experts = [g(a) for a in (w.w13, w.sf13, w.g13, w.w2, w.sf2, w.g2)]
+    else:
+        experts = [g(a) for a in (w.w13, w.s13, w.w2, w.s2)]
     x = torch.from_numpy(xb.astype(np.int16)).view(torch.bfloat16).to(dev)
     out = torch.empty_like(x)
     layer = MoELayer(T, fam.hidden, fam.n_experts, fam.inter, k, local_rank)
@@ -356,11 +378,14 @@ def run_native(args, rank, local_rank, world):
         flush_r.max()
 
     decode = T <= 64
-    path = layer.resolved_path(T)
+    path = "nvfp4-gemv" if fp4 else layer.resolved_path(T)
     dominant = "gate_up"
 
     def step():
-        layer.forward(x, rw, rb, w13, s13, w2, s2, k, out=out, stream=stream)
+        if fp4:
+            layer.forward_nvfp4(x, rw, rb, *experts, k, out=out, stream=stream)
+        else:
+            layer.forward(x, rw, rb, *experts, k, out=out, stream=stream)
 
     for _ in range(args.warmup):
         flush()
@@ -396,18 +421,28 @@ def run_native(args, rank, local_rank, world):
 
     kernels_us = kernel_breakdown(layer, step, flush, dev, 20 if decode else 5)
 
-    # end to end through the host-buffer entry point (pinned buffers)
+    # end to end with host buffers (pinned): the host-buffer entry point for
+    # FP8 experts; for FP4 experts the copies around the device entry point
     xh = torch.from_numpy(xb.astype(np.int16)).view(torch.bfloat16).pin_memory()
     oh = torch.empty_like(xh).pin_memory()
+
+    def e2e_step():
+        if fp4:
+            x.copy_(xh, non_blocking=True)
+            layer.forward_nvfp4(x, rw, rb, *experts, k, out=out, stream=stream)
+            oh.copy_(out, non_blocking=True)
+        else:
+            layer.forward_host(xh, rw, rb, *experts, k, oh, stream=stream)
+
     for _ in range(3):
-        layer.forward_host(xh, rw, rb, w13, s13, w2, s2, k, oh, stream=stream)
+        e2e_step()
     K2 = max(1, min(K, 500))
     e2e_ms = []
     for _ in range(K2):
         flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        layer.forward_host(xh, rw, rb, w13, s13, w2, s2, k, oh, stream=stream)
+        e2e_step()
         b.record(stream)
         b.synchronize()
         e2e_ms.append(a.elapsed_time(b))
@@ -418,10 +453,19 @@ def run_native(args, rank, local_rank, world):
         return None
 
     hbm, bf16, bf16_sus, src = peaks()
-    sb = selected_bytes(fam, counts)
+    sb = selected_bytes(fam, counts, args.format)
     P = T * k
     dom_s = dom_ms / max(dom_n, 1) / 1e3
-    if decode and path == "tcgemv":
+    if fp4:
+        # gate/up GEMV: selected experts' W13 codes and scales, x (f16) in,
+        # h (f32) out
+        dom_bytes = sb["w13"] + T * fam.hidden * 2 + P * fam.inter * 4
+        achieved = dom_bytes / dom_s / 1e9
+        roof = dict(bound="hbm", achieved=achieved, peak=hbm, unit="GB/s", frac=achieved / hbm,
+                    traffic=None, kernel="fp4_gate_up (NVFP4 grouped GEMV + SwiGLU)",
+                    algorithmic_bytes=dom_bytes, avg_launch_us=dom_s * 1e6,
+                    peak_source=f"hbm_gbs, {src}")
+    elif decode and path == "tcgemv":
         # one launch streams both projections: selected experts' W13 and W2
         # (codes and scales), the activations in and y out
         dom_bytes = sb["w13"] + sb["w2"] + T * fam.hidden * 2 + P * fam.hidden * 4
@@ -451,11 +495,14 @@ def run_native(args, rank, local_rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3 weights x f16 activations, f32 accumulate" if path == "gemv" else
+        "dtype": ("e2m1 (NVFP4) weights x f16 activations, f32 accumulate" if fp4 else
+                  "e4m3 weights x f16 activations, f32 accumulate" if path == "gemv" else
                   "e4m3 weights x multi-term e4m3 activations, f32 accumulate"),
-        "data": "synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised to "
-                "e4m3 per 128x128 block)",
-        "config": {"workload": args.workload, "tokens": T, "hidden": fam.hidden,
+        "data": ("synthetic (seeded N(0,1) bf16 activations, N(0,0.02) weights quantised to "
+                 + ("NVFP4: e2m1 + e4m3 scale per 16 + f32 per matrix)" if fp4 else
+                    "e4m3 per 128x128 block)")),
+        "config": {"workload": args.workload, "format": args.format, "tokens": T,
+                   "hidden": fam.hidden,
                    "experts": fam.n_experts, "top_k": k, "inter": fam.inter,
                    "active_experts": sb["n_active"],
                    "path": path,
@@ -502,7 +549,7 @@ def main():
     res = run_native(args, rank, local_rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = oracle_rate(args.workload, args.cpu_seconds)
+            res["cpu_baseline"] = oracle_rate(args.workload, args.cpu_seconds, args.format)
         print(json.dumps(res))
     if world > 1:
         import torch

@@ -52,6 +52,8 @@ def lib():
     sig = {
         "moe_init": ([ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(MoEConfig)], ctypes.c_int),
         "moe_layer_forward": ([vp, vp, i64, vp, vp, vp, vp, vp, vp, i32, vp, vp], ctypes.c_int),
+        "moe_layer_forward_nvfp4": ([vp, vp, i64, vp, vp, vp, vp, vp, vp, vp, vp, i32, vp, vp],
+                                    ctypes.c_int),
         "moe_layer_forward_host": ([vp, vp, i64, vp, vp, vp, vp, vp, vp, i32, vp, vp], ctypes.c_int),
         "moe_get_routing": ([vp, vp, vp, vp, vp, vp, vp, vp], ctypes.c_int),
         "moe_status": ([vp], ctypes.c_int),

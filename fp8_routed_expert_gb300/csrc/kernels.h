@@ -150,6 +150,19 @@ cudaError_t launch_combine(const float *y, int n_planes, int64_t plane, const in
                            const float *wts, int64_t T, int k, int64_t H, __nv_bfloat16 *out,
                            cudaStream_t s);
 
+// FP4 (NVFP4) experts: grouped GEMVs with e2m1 codes [rows, K/2], e4m3 group
+// scales [rows, K/16] and an f32 global scale per expert; h f32 [P, I] with
+// per-position |h| maxima (hmax, cleared by the routing), y f32 [P, H].
+cudaError_t launch_fp4_gate_up(const uint8_t *w13, const uint8_t *sf13, const float *g13,
+                               const __half *x16, const float *xscale, const int32_t *counts,
+                               const int32_t *offsets, const int32_t *perm, const int32_t *active,
+                               const int32_t *n_active, int k, int64_t T, int64_t H, int64_t I,
+                               float *h, uint32_t *hmax, int64_t max_items, int sms, cudaStream_t s);
+cudaError_t launch_fp4_down(const uint8_t *w2, const uint8_t *sf2, const float *g2, const float *h,
+                            const uint32_t *hmax, const int32_t *counts, const int32_t *offsets,
+                            const int32_t *active, const int32_t *n_active, int64_t T, int64_t H,
+                            int64_t I, float *y, int64_t max_items, int sms, cudaStream_t s);
+
 // One CTA whose waits (an mbarrier nothing arrives on, a global counter
 // nothing increments) run out after limit_ns each: records DEV_ERR_TIMEOUT in
 // *err and, if `which` is given, which waits gave up (bit 0 the mbarrier,

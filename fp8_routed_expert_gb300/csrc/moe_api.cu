@@ -139,6 +139,76 @@ int resolve_path(const moe_ctx *c, int64_t T) {
   return path;
 }
 
+// Routing for the grouped-GEMV and grouped-GEMM expert kernels: logits,
+// certified top-k, the pair sort with 128-position tiles; for the GEMV
+// kernels (gemv) also the f16 copy of x with its per-token power-of-two
+// scale and cleared per-position |h| maxima.
+int route_for_expert_kernels(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw,
+                             const float *rb, int k, bool gemv, cudaStream_t s) {
+  const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, P = T * k;
+  const int ks = router_k_split(T, E, H, c->sms);
+  const float gamma = router_gamma(T, H, ks);
+  if (T <= kRouterWarpMaxT) {
+    Timed tm(c, MOE_K_ROUTE, s);
+    CUDA_TRY(launch_route_decode(x, T, rw, rb, E, H, k, gamma, c->logits, c->wnorm, c->xnorm,
+                                 gemv ? c->x16 : nullptr, c->xscale, c->ticket, c->idx, c->wts,
+                                 c->counts, c->offsets, c->perm, c->inv, c->active, c->n_active,
+                                 c->tile_offsets, kTileM, gemv ? c->hmax : nullptr, c->err, s));
+    return MOE_OK;
+  }
+  {
+    Timed tm(c, MOE_K_ROUTER_LOGITS, s, 2);  // row norms, then the tiled logits
+    CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
+  }
+  {
+    Timed tm(c, MOE_K_ROUTER_SELECT, s);
+    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks, gamma, c->idx,
+                                  c->wts, c->err, s));
+  }
+  if (gemv) {
+    c->n_launches += 1;
+    CUDA_TRY(launch_x_to_f16(x, T, H, c->x16, c->xscale, s));
+  }
+  {
+    Timed tm(c, MOE_K_PERMUTE, s);
+    CUDA_TRY(launch_permute(c->idx, P, (int)E, kTileM, c->counts, c->offsets, c->perm, c->inv,
+                            c->active, c->n_active, c->tile_offsets, gemv ? c->hmax : nullptr,
+                            nullptr, 0, c->err, s));
+  }
+  return MOE_OK;
+}
+
+// The layer with FP4 experts: routing as for the GEMV kernels, the two FP4
+// grouped GEMVs, the rank-order combine.
+int forward_nvfp4(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw, const float *rb,
+                  const uint8_t *w13, const uint8_t *sf13, const float *g13, const uint8_t *w2,
+                  const uint8_t *sf2, const float *g2, int k, __nv_bfloat16 *out, cudaStream_t s) {
+  const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, I = c->cfg.inter, P = T * k;
+  const int64_t max_active = P < E ? P : E;
+  int rc = route_for_expert_kernels(c, x, T, rw, rb, k, true, s);
+  if (rc != MOE_OK) return rc;
+  {
+    Timed tm(c, MOE_K_GATE_UP, s);
+    CUDA_TRY(launch_fp4_gate_up(w13, sf13, g13, c->x16, c->xscale, c->counts, c->offsets, c->perm,
+                                c->active, c->n_active, k, T, H, I, c->h, c->hmax,
+                                max_active * (I / 8), c->sms, s));
+  }
+  {
+    Timed tm(c, MOE_K_DOWN, s);
+    CUDA_TRY(launch_fp4_down(w2, sf2, g2, c->h, c->hmax, c->counts, c->offsets, c->active,
+                             c->n_active, T, H, I, c->y, max_active * (H / 16), c->sms, s));
+  }
+  {
+    Timed tm(c, MOE_K_COMBINE, s);
+    CUDA_TRY(launch_combine(c->y, 1, 0, c->inv, c->wts, T, k, H, out, s));
+  }
+  c->last_T = T;
+  c->last_k = k;
+  c->last_stream = s;
+  if (c->timing && c->pending.size() > 16384) drain_timing(c);
+  return MOE_OK;
+}
+
 int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw,
                    const float *rb, const uint8_t *w13, const float *s13, const uint8_t *w2,
                    const float *s2, int k, __nv_bfloat16 *out, cudaStream_t s) {
@@ -201,35 +271,9 @@ int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *r
     return MOE_OK;
   }
   const int tile_m = kTileM;
-  const int ks = router_k_split(T, E, H, c->sms);
-  const float gamma = router_gamma(T, H, ks);
-  if (T <= kRouterWarpMaxT) {
-    Timed tm(c, MOE_K_ROUTE, s);
-    CUDA_TRY(launch_route_decode(x, T, rw, rb, E, H, k, gamma, c->logits, c->wnorm, c->xnorm,
-                                 path == MOE_PATH_GEMV ? c->x16 : nullptr, c->xscale, c->ticket,
-                                 c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv, c->active,
-                                 c->n_active, c->tile_offsets, tile_m,
-                                 path == MOE_PATH_GEMV ? c->hmax : nullptr, c->err, s));
-  } else {
-    {
-      Timed tm(c, MOE_K_ROUTER_LOGITS, s, 2);  // row norms, then the tiled logits
-      CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
-    }
-    {
-      Timed tm(c, MOE_K_ROUTER_SELECT, s);
-      CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks, gamma, c->idx,
-                                    c->wts, c->err, s));
-    }
-    if (path == MOE_PATH_GEMV) {
-      c->n_launches += 1;
-      CUDA_TRY(launch_x_to_f16(x, T, H, c->x16, c->xscale, s));
-    }
-    {
-      Timed tm(c, MOE_K_PERMUTE, s);
-      CUDA_TRY(launch_permute(c->idx, P, (int)E, tile_m, c->counts, c->offsets, c->perm, c->inv,
-                              c->active, c->n_active, c->tile_offsets,
-                              path == MOE_PATH_GEMV ? c->hmax : nullptr, nullptr, 0, c->err, s));
-    }
+  {
+    const int rc = route_for_expert_kernels(c, x, T, rw, rb, k, path == MOE_PATH_GEMV, s);
+    if (rc != MOE_OK) return rc;
   }
   if (path == MOE_PATH_GEMV) {
     {
@@ -445,6 +489,26 @@ int moe_layer_forward(moe_ctx *c, const void *hidden, int64_t T, const float *rw
   if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
   return forward_device(c, (const __nv_bfloat16 *)hidden, T, rw, rb, w13, s13, w2, s2, top_k,
                         (__nv_bfloat16 *)out, (cudaStream_t)stream);
+}
+
+int moe_layer_forward_nvfp4(moe_ctx *c, const void *hidden, int64_t T, const float *rw,
+                            const float *rb, const uint8_t *w13, const uint8_t *sf13,
+                            const float *g13, const uint8_t *w2, const uint8_t *sf2,
+                            const float *g2, int32_t top_k, void *out, void *stream) {
+  // shapes, T and k as for the FP8 entry point (the scale arguments are
+  // checked there for 4-byte alignment; here the group scales need 2)
+  int rc = check_forward_args(c, hidden, T, rw, rb, w13, g13, w2, g2, top_k, out);
+  if (rc != MOE_OK) return rc;
+  if (T == 0) {
+    c->last_T = 0;
+    c->last_k = top_k;
+    return MOE_OK;
+  }
+  if (!sf13 || !sf2) return MOE_ERR_ARG;
+  if (!aligned(sf13, 2) || !aligned(sf2, 2)) return MOE_ERR_ALIGN;
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  return forward_nvfp4(c, (const __nv_bfloat16 *)hidden, T, rw, rb, w13, sf13, g13, w2, sf2, g2,
+                       top_k, (__nv_bfloat16 *)out, (cudaStream_t)stream);
 }
 
 int moe_layer_forward_host(moe_ctx *c, const void *hidden_host, int64_t T, const float *rw,

@@ -80,6 +80,33 @@ class MoELayer:
         check(rc, "moe_layer_forward")
         return out
 
+    def forward_nvfp4(self, x: torch.Tensor, router_w, router_bias, w13, sf13, g13, w2, sf2, g2,
+                      top_k: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        """The layer with FP4 (NVFP4) experts: w13 u8 [E, 2I, H/2], sf13 u8
+        [E, 2I, H/16], g13 f32 [E]; w2 u8 [E, H, I/2], sf2 u8 [E, H, I/16],
+        g2 f32 [E] (see include/fp8moe.h).  Returns bf16 [T, H]."""
+        c = self.cfg
+        E, H, I = c.n_experts, c.hidden, c.inter
+        if x.dtype != torch.bfloat16 or x.dim() != 2 or x.shape[1] != H or not x.is_contiguous():
+            raise ValueError("x must be a contiguous bf16 [T, H] tensor")
+        want = [(router_w, torch.float32, (E, H)), (w13, torch.uint8, (E, 2 * I, H // 2)),
+                (sf13, torch.uint8, (E, 2 * I, H // 16)), (g13, torch.float32, (E,)),
+                (w2, torch.uint8, (E, H, I // 2)), (sf2, torch.uint8, (E, H, I // 16)),
+                (g2, torch.float32, (E,))]
+        if router_bias is not None:
+            want.append((router_bias, torch.float32, (E,)))
+        for t, dt, shape in want:
+            if t.dtype != dt or tuple(t.shape) != shape or not t.is_contiguous() or not t.is_cuda:
+                raise ValueError(f"expected contiguous cuda {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
+        if out is None:
+            out = torch.empty_like(x)
+        rc = lib().moe_layer_forward_nvfp4(self._h, _ptr(x), x.shape[0], _ptr(router_w),
+                                           _ptr(router_bias), _ptr(w13), _ptr(sf13), _ptr(g13),
+                                           _ptr(w2), _ptr(sf2), _ptr(g2), top_k, _ptr(out),
+                                           _stream_handle(stream))
+        check(rc, "moe_layer_forward_nvfp4")
+        return out
+
     def forward_host(self, x_host: torch.Tensor, router_w, router_bias, w13, s13, w2, s2,
                      top_k: int, out_host: torch.Tensor, stream=None) -> torch.Tensor:
         """x_host, out_host: bf16 [T, H] CPU tensors (pinned for async copies)."""

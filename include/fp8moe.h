@@ -114,6 +114,30 @@ int moe_layer_forward_host(moe_ctx *ctx, const void *hidden_host, int64_t T,
                            void *out_host, void *stream);
 
 /*
+ * moe_layer_forward_nvfp4 - the same layer (steps 1-5 above) with FP4 expert
+ * weights in the NVFP4 format of the Qwen post's experts ("Why this model, of
+ * all models"; "The engine", piece 1: half a byte per weight plus one e4m3
+ * scale per 16 weights; piece 4: the e2m1 -> f16x2 hardware conversion).  A
+ * weight's value is e2m1(code) * e4m3(group scale) * global scale.  The
+ * router, hidden, out, top_k and stream arguments are those of
+ * moe_layer_forward.
+ *   w13  : device, u8 [E, 2I, H/2]: e2m1 codes of W13 (rows [0,I) gate,
+ *          [I,2I) up), two per byte along H, element 2j in the low nibble;
+ *          16-byte aligned.
+ *   sf13 : device, u8 [E, 2I, H/16]: e4m3 scale of each 16 consecutive
+ *          weights of a row; 2-byte aligned.
+ *   g13  : device, f32 [E]: global scale of each expert's W13; 4-byte aligned.
+ *   w2, sf2, g2 : the same for W2 [E, H, I] (codes [E, H, I/2], scales
+ *          [E, H, I/16], globals [E]).
+ * The expert kernels are grouped GEMVs (any T; built for small batches).
+ * Errors as for moe_layer_forward; sf13 / sf2 NULL is MOE_ERR_ARG.
+ */
+int moe_layer_forward_nvfp4(moe_ctx *ctx, const void *hidden, int64_t T, const float *router_w,
+                            const float *router_bias, const uint8_t *w13, const uint8_t *sf13,
+                            const float *g13, const uint8_t *w2, const uint8_t *sf2,
+                            const float *g2, int32_t top_k, void *out, void *stream);
+
+/*
  * moe_get_routing - copy the routing of the last forward into caller device
  * buffers (any may be NULL to skip it).  Sizes for that forward's T and k,
  * P = T*k:
