@@ -114,6 +114,7 @@ __global__ void __launch_bounds__(32 * kFp4Warps) fp4_gate_up_kernel(
     const int cnt = counts[e], off = offsets[e];
     const float ge = g13[e];
     for (int n0 = 0; n0 < cnt; n0 += 8 * NG) {
+      const int ngroups = (cnt - n0 + 7) / 8;  // groups of 8 positions with work in this pass
       // B rows: position n0 + 8 ng + g of this pass (a zero row past the segment)
       const __half *xr[NG];
 #pragma unroll
@@ -145,6 +146,7 @@ __global__ void __launch_bounds__(32 * kFp4Warps) fp4_gate_up_kernel(
           chunk_fragments(wa[u], wb[u], sca[u], scb[u], a);
 #pragma unroll
           for (int ng = 0; ng < NG; ++ng) {
+            if (ng >= ngroups) break;  // warp-uniform: groups past the segment hold no position
             const __half *xp = xr[ng] ? xr[ng] + (kc0 + u) * 128 : nullptr;
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
@@ -200,6 +202,7 @@ __global__ void __launch_bounds__(32 * kFp4Warps) fp4_down_kernel(
     const int cnt = counts[e], off = offsets[e];
     const float ge = g2[e];
     for (int n0 = 0; n0 < cnt; n0 += 8 * NG) {
+      const int ngroups = (cnt - n0 + 7) / 8;
       const float *hr[NG];
       float down[NG];
 #pragma unroll
@@ -232,6 +235,7 @@ __global__ void __launch_bounds__(32 * kFp4Warps) fp4_down_kernel(
           chunk_fragments(wa[u], wb[u], sca[u], scb[u], a);
 #pragma unroll
           for (int ng = 0; ng < NG; ++ng) {
+            if (ng >= ngroups) break;  // warp-uniform
             const float *hp = hr[ng] ? hr[ng] + (kc0 + u) * 128 : nullptr;
 #pragma unroll
             for (int s = 0; s < 8; ++s) {

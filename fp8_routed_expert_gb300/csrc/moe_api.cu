@@ -185,8 +185,23 @@ int forward_nvfp4(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw
                   const uint8_t *sf2, const float *g2, int k, __nv_bfloat16 *out, cudaStream_t s) {
   const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, I = c->cfg.inter, P = T * k;
   const int64_t max_active = P < E ? P : E;
-  int rc = route_for_expert_kernels(c, x, T, rw, rb, k, true, s);
-  if (rc != MOE_OK) return rc;
+  if (T <= kRouterWarpMaxT) {
+    // the two-kernel small-batch routing (it also clears the per-position
+    // |h| maxima), then the f16 copy of x
+    const int64_t Pm = c->cfg.max_tokens * c->cfg.max_top_k;
+    {
+      Timed tm(c, MOE_K_ROUTE, s, 2);
+      CUDA_TRY(launch_route_small(x, T, rw, rb, E, H, k, c->logits, c->wnorm, c->xss, c->a_hi,
+                                  c->a_lo, c->a_scale, Pm, reinterpret_cast<int32_t *>(c->hmax),
+                                  (int)P, c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv,
+                                  c->active, c->n_active, c->tile_offsets, kTileM, c->err, s));
+    }
+    c->n_launches += 1;
+    CUDA_TRY(launch_x_to_f16(x, T, H, c->x16, c->xscale, s));
+  } else {
+    const int rc = route_for_expert_kernels(c, x, T, rw, rb, k, true, s);
+    if (rc != MOE_OK) return rc;
+  }
   {
     Timed tm(c, MOE_K_GATE_UP, s);
     CUDA_TRY(launch_fp4_gate_up(w13, sf13, g13, c->x16, c->xscale, c->counts, c->offsets, c->perm,
