@@ -71,6 +71,13 @@ def parse():
     ap.add_argument("--format", default="fp8", choices=["fp8", "nvfp4"],
                     help="expert weight format: blockwise e4m3 (default) or NVFP4 (e2m1 + e4m3 "
                          "scale per 16 weights + f32 global per expert matrix)")
+    ap.add_argument("--expert-cache", type=int, default=0, metavar="SLOTS",
+                    help="stream the experts from host memory through a cache of SLOTS experts "
+                         "per layer, over a stack of --layers layers (decode batches)")
+    ap.add_argument("--layers", type=int, default=16)
+    ap.add_argument("--guesses", type=int, default=0,
+                    help="experts of the next layer to prefetch, guessed with its router on "
+                         "this layer's input (default: top_k)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -524,6 +531,96 @@ def run_native(args, rank, local_rank, world):
     return res
 
 
+def run_stream(args) -> dict:
+    """Decode through a stack of layers whose experts live in host memory.
+
+    Layer l has its own seeded weights (seed * 100 + l); x_{l+1} = x_l +
+    MoE_l(x_l).  Three ways are timed over the same token batches: every
+    expert resident in device memory; the expert cache (SLOTS per layer,
+    copies over NVLink-C2C when an expert is missing); the cache with the
+    next layer's experts guessed from its router on this layer's input and
+    prefetched while this layer computes."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from fp8_routed_expert_gb300 import ExpertCache, MoELayer
+
+    fam, T = W.parse_workload(args.workload)
+    k, L, slots = fam.top_k, args.layers, args.expert_cache
+    n_guess = args.guesses or k
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    layers = []
+    for l in range(L):
+        f = W.Family(fam.name, fam.hidden, fam.n_experts, fam.top_k, fam.inter, fam.seed * 100 + l,
+                     fam.tokens, fam.bias_std)
+        w = W.make_weights(f)
+        layers.append(dict(
+            rw=g(w.router_w), rb=None if w.router_bias is None else g(w.router_bias),
+            s13=g(w.s13), s2=g(w.s2), w13_host=torch.from_numpy(w.w13), w2_host=torch.from_numpy(w.w2),
+            w13=g(w.w13), w2=g(w.w2),
+            ctx=MoELayer(T, fam.hidden, fam.n_experts, fam.inter, k, 0)))
+    for ly in layers:
+        ly["cache"] = ExpertCache(ly["ctx"], ly["w13_host"], ly["w2_host"], slots)
+    xs = [torch.from_numpy(W.normal_bf16(9000 + i, W.configs.TID_X, (T, fam.hidden)).astype(np.int16))
+          .view(torch.bfloat16).to(dev) for i in range(args.steps + args.warmup)]
+
+    def token_step(x, mode):
+        for l, ly in enumerate(layers):
+            if mode == "resident":
+                out = ly["ctx"].forward(x, ly["rw"], ly["rb"], ly["w13"], ly["s13"], ly["w2"],
+                                        ly["s2"], k, stream=stream)
+            else:
+                out = ly["cache"].forward(x, ly["rw"], ly["rb"], ly["s13"], ly["s2"], k, stream=stream)
+                if mode == "prefetch" and l + 1 < L:
+                    nxt = layers[l + 1]
+                    nxt["cache"].prefetch(nxt["cache"].guess(x, nxt["rw"], nxt["rb"], k, n_guess))
+            x = x + out
+        return x
+
+    res = {}
+    for mode in ("resident", "cache", "prefetch"):
+        before = [ly["cache"].stats() for ly in layers]
+        for i in range(args.warmup):
+            token_step(xs[i], mode)
+        torch.cuda.synchronize(dev)
+        mid = [ly["cache"].stats() for ly in layers]
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            token_step(xs[args.warmup + i], mode)
+        torch.cuda.synchronize(dev)
+        el = time.perf_counter() - t0
+        after = [ly["cache"].stats() for ly in layers]
+        d = {key: sum(a[key] - m[key] for a, m in zip(after, mid)) for key in after[0]}
+        res[mode] = dict(tokens_s=T * args.steps / el, ms_per_token_step=el / args.steps * 1e3,
+                         **{f"{kk}": v for kk, v in d.items()})
+        del before
+    hbm, _, _, src = peaks()
+    pf, ca = res["prefetch"], res["cache"]
+    lookups = lambda r: r["hits"] + r["misses"]
+    return {
+        "metric": METRIC, "value": pf["tokens_s"], "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": pf["ms_per_token_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 weights x multi-term e4m3 activations, f32 accumulate",
+        "data": "synthetic (seeded per layer; a new token batch every step)",
+        "config": {"workload": f"{args.workload} through {L} layers, experts in host memory",
+                   "layers": L, "slots_per_layer": slots, "experts_per_layer": fam.n_experts,
+                   "guesses": n_guess, "expert_bytes": 3 * fam.hidden * fam.inter,
+                   "host_expert_bytes": L * fam.n_experts * 3 * fam.hidden * fam.inter},
+        "stream": {
+            "resident_tokens_s": res["resident"]["tokens_s"],
+            "cache_tokens_s": ca["tokens_s"], "cache_prefetch_tokens_s": pf["tokens_s"],
+            "cache_hit_rate": ca["hits"] / max(lookups(ca), 1),
+            "prefetch_hit_rate": pf["hits"] / max(lookups(pf), 1),
+            "prefetched_used_frac": pf["prefetch_used"] / max(pf["prefetched"], 1),
+            "c2c_gbs_cache": ca["bytes_copied"] / (ca["ms_per_token_step"] * args.steps / 1e3) / 1e9,
+            "c2c_gbs_prefetch": pf["bytes_copied"] / (pf["ms_per_token_step"] * args.steps / 1e3) / 1e9,
+            "per_mode": res},
+    }
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
@@ -538,6 +635,11 @@ def main():
         print(json.dumps(r))
         return 0
 
+    if args.expert_cache:
+        args.steps = args.steps or 50
+        args.warmup = max(args.warmup or 5, 3)
+        print(json.dumps(run_stream(args)))
+        return 0
     if args.steps is None:
         args.steps = 3000 if T <= 64 else 200
     if args.warmup is None:

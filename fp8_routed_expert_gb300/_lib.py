@@ -67,6 +67,13 @@ def lib():
         "moe_kernel_name": ([ctypes.c_int], ctypes.c_char_p),
         "moe_launch_count": ([vp], ctypes.c_int64),
         "moe_selftest_wait_timeout": ([vp, i64, vp, vp], ctypes.c_int),
+        "moe_cache_init": ([ctypes.POINTER(ctypes.c_void_p), vp, vp, vp, i64], ctypes.c_int),
+        "moe_cache_forward": ([vp, vp, i64, vp, vp, vp, vp, i32, vp, vp], ctypes.c_int),
+        "moe_cache_prefetch": ([vp, vp, i64], ctypes.c_int),
+        "moe_cache_guess": ([vp, vp, i64, vp, vp, i32, i32, vp], ctypes.c_int),
+        "moe_cache_stats": ([vp, vp, i32], ctypes.c_int),
+        "moe_cache_resident": ([vp, vp], ctypes.c_int),
+        "moe_cache_free": ([vp], None),
         "moe_route_noalloc": ([vp, i64, i64, vp, vp, i64, i32, vp, vp, vp, vp, vp, vp, vp],
                               ctypes.c_int),
         "moe_debug_copy": ([vp, ctypes.c_char_p, vp, i64, ctypes.POINTER(ctypes.c_int64), vp],

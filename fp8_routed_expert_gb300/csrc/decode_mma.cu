@@ -103,6 +103,7 @@ struct FfnArgs {
   int32_t *done13;                        // finished gate/up items per tile (0 at entry)
   int32_t *queue;                         // items handed out so far (0 at entry)
   int *err;
+  const int32_t *slot_of;                 // weight slab of each expert, or nullptr (slab = expert)
 };
 
 struct DItem {
@@ -304,8 +305,9 @@ __global__ void __launch_bounds__(DTHREADS, 1) decode_ffn_kernel(const __grid_co
       if (end) break;
       const bool dn = wk.down(item);
       const DItem c = ditem(s_toff, s_off, p.E, wk.nblocks(item), wk.local(item));
-      const int64_t r0 = dn ? (int64_t)c.e * p.H + (int64_t)c.nb * 256       // 256 W2 rows
-                            : (int64_t)c.e * 2 * p.I + (int64_t)c.nb * 128;  // 128 gate rows
+      const int64_t ws = p.slot_of ? __ldg(p.slot_of + c.e) : c.e;      // weight slab
+      const int64_t r0 = dn ? ws * p.H + (int64_t)c.nb * 256         // 256 W2 rows
+                            : ws * 2 * p.I + (int64_t)c.nb * 128;    // 128 gate rows
       const int64_t nkb = dn ? nkb2 : nkb1;
       int next = 0;
       for (int64_t kb = 0; kb < nkb; ++kb) {
@@ -661,9 +663,9 @@ cudaError_t launch_decode_ffn(const DecodeMaps &maps, const int32_t *offsets,
                               const float *x_scale, int64_t x_ld, const float *s13, const float *s2,
                               int E, int64_t H, int64_t I, int64_t Pmax, uint8_t *const h_terms[3],
                               float *h_scale, float *y, int64_t y_plane, int32_t *done13, int *err,
-                              int64_t max_tiles,
-                              int sms, cudaStream_t s) {
+                              int64_t max_tiles, int sms, cudaStream_t s, const int32_t *slot_of) {
   FfnArgs p;
+  p.slot_of = slot_of;
   p.offsets = offsets;
   p.tile_offsets = tile_offsets;
   p.perm = perm;

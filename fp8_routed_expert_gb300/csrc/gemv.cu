@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv13_swiglu_kernel(
     const float *__restrict__ xscale, const int32_t *__restrict__ counts,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ perm,
     const int32_t *__restrict__ active, const int32_t *__restrict__ n_active, int k, int64_t H,
-    int64_t I, int64_t tb0, float *__restrict__ h, uint32_t *__restrict__ hmax) {
+    int64_t I, int64_t tb0, float *__restrict__ h, uint32_t *__restrict__ hmax,
+    const int32_t *__restrict__ slot_of) {
   extern __shared__ __align__(128) uint8_t ring_all[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
@@ -137,8 +138,9 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv13_swiglu_kernel(
   const uint8_t *is_gate = nullptr;
   auto issue_item = [&]() {
     const int e = active[is_item / ipe];
+    const int64_t ws = slot_of ? __ldg(slot_of + e) : e;  // weight slab of the expert
     const int64_t i0 = (int64_t)(is_item % ipe) * 8;
-    is_gate = w13 + ((int64_t)e * 2 * I + i0 + cl.rpar) * H + cl.col * 16;
+    is_gate = w13 + (ws * 2 * I + i0 + cl.rpar) * H + cl.col * 16;
   };
   issue_item();
   const int64_t up_off = I * H, two_rows = 2 * H;
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv2_kernel(
     const uint32_t *__restrict__ hmax, const int32_t *__restrict__ counts,
     const int32_t *__restrict__ offsets, const int32_t *__restrict__ active,
     const int32_t *__restrict__ n_active, int64_t H, int64_t I, int64_t tb0,
-    float *__restrict__ y) {
+    float *__restrict__ y, const int32_t *__restrict__ slot_of) {
   extern __shared__ __align__(128) uint8_t ring_all[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
@@ -287,8 +289,9 @@ __global__ void __launch_bounds__(32 * kGemvWarps) gemv2_kernel(
   const uint8_t *is_row = nullptr;
   auto issue_item = [&]() {
     const int e = active[is_item / ipe];
+    const int64_t ws = slot_of ? __ldg(slot_of + e) : e;  // weight slab of the expert
     const int64_t j0 = (int64_t)(is_item % ipe) * 16;
-    is_row = w2 + ((int64_t)e * H + j0 + cl.rpar) * I + cl.col * 16;
+    is_row = w2 + (ws * H + j0 + cl.rpar) * I + cl.col * 16;
   };
   issue_item();
   const int64_t two_rows = 2 * I;
@@ -492,7 +495,8 @@ cudaError_t launch_gemv13(const uint8_t *w13, const float *s13, const __half *x1
                           const float *xscale, const int32_t *counts, const int32_t *offsets,
                           const int32_t *perm, const int32_t *active, const int32_t *n_active,
                           int k, int64_t T, int64_t H, int64_t I, float *h, uint32_t *hmax,
-                          int64_t max_items, int *err, int sms, cudaStream_t s) {
+                          int64_t max_items, int *err, int sms, cudaStream_t s,
+                          const int32_t *slot_of) {
   cudaError_t e;
   if (T <= 8) {
     auto kern = gemv13_swiglu_kernel<1>;
@@ -500,7 +504,8 @@ cudaError_t launch_gemv13(const uint8_t *w13, const float *s13, const __half *x1
     const int64_t grid = gemv_grid(kern, max_items, sms);
     if (grid <= 0) return cudaSuccess;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(32 * kGemvWarps), kGemvSmem, s, w13, s13, x16,
-                      xscale, counts, offsets, perm, active, n_active, k, H, I, (int64_t)0, h, hmax);
+                      xscale, counts, offsets, perm, active, n_active, k, H, I, (int64_t)0, h, hmax,
+                      slot_of);
   }
   auto kern = gemv13_swiglu_kernel<8>;
   if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
@@ -509,14 +514,15 @@ cudaError_t launch_gemv13(const uint8_t *w13, const float *s13, const __half *x1
   for (int64_t tb0 = 0; tb0 < T; tb0 += 64)
     kern<<<(unsigned)grid, 32 * kGemvWarps, kGemvSmem, s>>>(w13, s13, x16, xscale, counts, offsets,
                                                             perm, active, n_active, k, H, I, tb0, h,
-                                                            hmax);
+                                                            hmax, slot_of);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, const uint32_t *hmax,
                          const int32_t *counts, const int32_t *offsets, const int32_t *active,
                          const int32_t *n_active, int64_t T, int64_t H, int64_t I, float *y,
-                         int64_t max_items, int *err, int sms, cudaStream_t s) {
+                         int64_t max_items, int *err, int sms, cudaStream_t s,
+                         const int32_t *slot_of) {
   cudaError_t e;
   if (T <= 8) {
     auto kern = gemv2_kernel<1>;
@@ -524,7 +530,7 @@ cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, con
     const int64_t grid = gemv_grid(kern, max_items, sms);
     if (grid <= 0) return cudaSuccess;
     return launch_pdl(kern, dim3((unsigned)grid), dim3(32 * kGemvWarps), kGemvSmem, s, w2, s2, h, hmax,
-                      counts, offsets, active, n_active, H, I, (int64_t)0, y);
+                      counts, offsets, active, n_active, H, I, (int64_t)0, y, slot_of);
   }
   auto kern = gemv2_kernel<8>;
   if ((e = allow_smem(kern, kGemvSmem)) != cudaSuccess) return e;
@@ -532,7 +538,7 @@ cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, con
   if (grid <= 0) return cudaSuccess;
   for (int64_t tb0 = 0; tb0 < T; tb0 += 64)
     kern<<<(unsigned)grid, 32 * kGemvWarps, kGemvSmem, s>>>(w2, s2, h, hmax, counts, offsets,
-                                                            active, n_active, H, I, tb0, y);
+                                                            active, n_active, H, I, tb0, y, slot_of);
   return cudaGetLastError();
 }
 

@@ -76,11 +76,13 @@ cudaError_t launch_gemv13(const uint8_t *w13, const float *s13, const __half *x1
                           const float *xscale, const int32_t *counts, const int32_t *offsets,
                           const int32_t *perm, const int32_t *active, const int32_t *n_active,
                           int k, int64_t T, int64_t H, int64_t I, float *h, uint32_t *hmax,
-                          int64_t max_items, int *err, int sms, cudaStream_t s);
+                          int64_t max_items, int *err, int sms, cudaStream_t s,
+                          const int32_t *slot_of = nullptr);
 cudaError_t launch_gemv2(const uint8_t *w2, const float *s2, const float *h, const uint32_t *hmax,
                          const int32_t *counts, const int32_t *offsets, const int32_t *active,
                          const int32_t *n_active, int64_t T, int64_t H, int64_t I, float *y,
-                         int64_t max_items, int *err, int sms, cudaStream_t s);
+                         int64_t max_items, int *err, int sms, cudaStream_t s,
+                         const int32_t *slot_of = nullptr);
 bool encode_u8_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows);
 cudaError_t launch_act_quant(const __nv_bfloat16 *x, const int32_t *perm, int64_t P, int k,
                              int64_t H, int64_t Pmax, uint8_t *a_hi, uint8_t *a_lo, float *a_scale,
@@ -99,11 +101,15 @@ bool encode_h_store_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_
 bool encode_y_store_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows);
 // mode 1: gate/up + SwiGLU -> three-term e4m3 h (two activation terms in);
 // mode 2: down -> f32 y (three activation terms in).
+// slot_of (here and in the other expert kernels): when given, expert e's
+// weight codes are slab slot_of[e] of the weight tensors (an expert cache);
+// its block scales stay at index e.
 cudaError_t launch_grouped_gemm(int mode, const TmapSet &tm, const int32_t *offsets,
                                 const int32_t *tile_offsets, const float *a_scale,
                                 const float *w_scale, int E, int64_t H, int64_t I, int64_t Pmax,
                                 uint8_t *const h_terms[3], float *h_scale, float *y, int *err,
-                                int64_t max_items, int sms, cudaStream_t s);
+                                int64_t max_items, int sms, cudaStream_t s,
+                                const int32_t *slot_of = nullptr);
 // Positions per tile of the tensor-core decode FFN.
 constexpr int kDecodeTileN = 16;
 // Tensor maps of the decode FFN: weights (W13 boxes of 128 rows, W2 boxes of
@@ -127,7 +133,8 @@ cudaError_t launch_decode_ffn(const DecodeMaps &maps, const int32_t *offsets,
                               const float *x_scale, int64_t x_ld, const float *s13, const float *s2,
                               int E, int64_t H, int64_t I, int64_t Pmax, uint8_t *const h_terms[3],
                               float *h_scale, float *y, int64_t y_plane, int32_t *done13, int *err,
-                              int64_t max_tiles, int sms, cudaStream_t s);
+                              int64_t max_tiles, int sms, cudaStream_t s,
+                              const int32_t *slot_of = nullptr);
 // Per-token activation terms (two e4m3 terms, one power-of-two scale per
 // (token, 128 columns)); the token-major operand of the decode FFN.
 cudaError_t launch_act_quant_tokens(const __nv_bfloat16 *x, int64_t T, int64_t H, uint8_t *a_hi,

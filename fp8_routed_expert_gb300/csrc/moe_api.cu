@@ -8,6 +8,7 @@
 
 #include "fp8moe.h"
 #include "common.cuh"
+#include "ctx_internal.h"
 #include "kernels.h"
 
 using namespace fp8moe;
@@ -224,120 +225,137 @@ int forward_nvfp4(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw
   return MOE_OK;
 }
 
-int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw,
-                   const float *rb, const uint8_t *w13, const float *s13, const uint8_t *w2,
-                   const float *s2, int k, __nv_bfloat16 *out, cudaStream_t s) {
-  const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, I = c->cfg.inter;
+// Routing of the expert path `path`: everything before the expert kernels
+// (for the tensor-core decode path also the activation terms).
+int route_phase(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw, const float *rb,
+                int k, int path, cudaStream_t s) {
+  const int64_t E = c->cfg.n_experts, H = c->cfg.hidden;
   const int64_t P = T * k, Pm = c->cfg.max_tokens * c->cfg.max_top_k;
-  const int path = resolve_path(c, T);
+  const int64_t max_active = P < E ? P : E;
+  if (path != MOE_PATH_TCGEMV) return route_for_expert_kernels(c, x, T, rw, rb, k, path == MOE_PATH_GEMV, s);
+  const int64_t max_tiles = (P + kDecodeTileN - 1) / kDecodeTileN + max_active;
+  if (T <= kRouterWarpMaxT) {
+    Timed tm(c, MOE_K_ROUTE, s, 2);  // logits, then selection + sort
+    CUDA_TRY(launch_route_small(x, T, rw, rb, E, H, k, c->logits, c->wnorm, c->xss, c->a_hi,
+                                c->a_lo, c->a_scale, Pm, c->done13, (int)max_tiles + 1,
+                                c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv, c->active,
+                                c->n_active, c->tile_offsets, kDecodeTileN, c->err, s));
+    return MOE_OK;
+  }
+  const int ks = router_k_split(T, E, H, c->sms);
+  {
+    Timed tm(c, MOE_K_ROUTER_LOGITS, s, 2);  // row norms, then the tiled logits
+    CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
+  }
+  {
+    Timed tm(c, MOE_K_ROUTER_SELECT, s);
+    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks,
+                                  router_gamma(T, H, ks), c->idx, c->wts, c->err, s));
+  }
+  {
+    Timed tm(c, MOE_K_PERMUTE, s);
+    CUDA_TRY(launch_permute(c->idx, P, (int)E, kDecodeTileN, c->counts, c->offsets, c->perm,
+                            c->inv, c->active, c->n_active, c->tile_offsets, nullptr, c->done13,
+                            (int)max_tiles + 1, c->err, s));
+  }
+  {
+    Timed tm(c, MOE_K_ACT_QUANT, s);
+    CUDA_TRY(launch_act_quant_tokens(x, T, H, c->a_hi, c->a_lo, c->a_scale, Pm, c->sms, s));
+  }
+  return MOE_OK;
+}
+
+// The expert kernels of path `path` and the combine, on the routing that
+// route_phase left in the context.
+// slot_of / n_slabs: when slot_of is given, w13 and w2 hold n_slabs expert
+// slabs and expert e's codes are slab slot_of[e] (an expert cache).
+int expert_phase(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const uint8_t *w13,
+                 const float *s13, const uint8_t *w2, const float *s2, int k, int path,
+                 __nv_bfloat16 *out, cudaStream_t s, const int32_t *slot_of = nullptr,
+                 int64_t n_slabs = 0) {
+  const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, I = c->cfg.inter;
+  const int64_t NS = slot_of ? n_slabs : E;  // weight slabs the tensor maps cover
+  const int64_t P = T * k, Pm = c->cfg.max_tokens * c->cfg.max_top_k;
   const int64_t max_active = P < E ? P : E;
   if (path == MOE_PATH_TCGEMV) {
     const int64_t max_tiles = (P + kDecodeTileN - 1) / kDecodeTileN + max_active;
-    if (T <= kRouterWarpMaxT) {
-      Timed tm(c, MOE_K_ROUTE, s, 2);  // logits, then selection + sort
-      CUDA_TRY(launch_route_small(x, T, rw, rb, E, H, k, c->logits, c->wnorm, c->xss, c->a_hi,
-                                  c->a_lo, c->a_scale, Pm, c->done13, (int)max_tiles + 1,
-                                  c->idx, c->wts, c->counts, c->offsets, c->perm, c->inv, c->active,
-                                  c->n_active, c->tile_offsets, kDecodeTileN, c->err, s));
-    } else {
-      const int ks = router_k_split(T, E, H, c->sms);
-      {
-        Timed tm(c, MOE_K_ROUTER_LOGITS, s, 2);  // row norms, then the tiled logits
-        CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
-      }
-      {
-        Timed tm(c, MOE_K_ROUTER_SELECT, s);
-        CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks,
-                                      router_gamma(T, H, ks), c->idx, c->wts, c->err, s));
-      }
-      {
-        Timed tm(c, MOE_K_PERMUTE, s);
-        CUDA_TRY(launch_permute(c->idx, P, (int)E, kDecodeTileN, c->counts, c->offsets, c->perm,
-                                c->inv, c->active, c->n_active, c->tile_offsets, nullptr, c->done13,
-                                (int)max_tiles + 1, c->err, s));
-      }
-      {
-        Timed tm(c, MOE_K_ACT_QUANT, s);
-        CUDA_TRY(launch_act_quant_tokens(x, T, H, c->a_hi, c->a_lo, c->a_scale, Pm, c->sms, s));
-      }
-    }
     if (c->dmaps_w13 != w13) {
-      if (!encode_u8_tmap(&c->dmaps.w13, w13, H, E * 2 * I, 128)) return MOE_ERR_CUDA;
+      if (!encode_u8_tmap(&c->dmaps.w13, w13, H, NS * 2 * I, 128)) return MOE_ERR_CUDA;
       c->dmaps_w13 = w13;
     }
     if (c->dmaps_w2 != w2) {
-      if (!encode_u8_tmap(&c->dmaps.w2, w2, I, E * H, 256)) return MOE_ERR_CUDA;
+      if (!encode_u8_tmap(&c->dmaps.w2, w2, I, NS * H, 256)) return MOE_ERR_CUDA;
       c->dmaps_w2 = w2;
     }
     {
       Timed tm(c, MOE_K_GATE_UP, s);
       CUDA_TRY(launch_decode_ffn(c->dmaps, c->offsets, c->tile_offsets, c->perm, k, c->a_scale, Pm,
                                  s13, s2, (int)E, H, I, Pm, c->h_t, c->h_scale, c->y, P * H,
-                                 c->done13, c->err, max_tiles, c->sms, s));
+                                 c->done13, c->err, max_tiles, c->sms, s, slot_of));
     }
     {
       Timed tm(c, MOE_K_COMBINE, s);
       CUDA_TRY(launch_combine(c->y, 3, P * H, c->inv, c->wts, T, k, H, out, s));
     }
-    c->last_T = T;
-    c->last_k = k;
-    c->last_stream = s;
-    if (c->timing && c->pending.size() > 16384) drain_timing(c);
-    return MOE_OK;
-  }
-  const int tile_m = kTileM;
-  {
-    const int rc = route_for_expert_kernels(c, x, T, rw, rb, k, path == MOE_PATH_GEMV, s);
-    if (rc != MOE_OK) return rc;
-  }
-  if (path == MOE_PATH_GEMV) {
-    {
-      Timed tm(c, MOE_K_GATE_UP, s);
-      CUDA_TRY(launch_gemv13(w13, s13, c->x16, c->xscale, c->counts, c->offsets, c->perm,
-                             c->active, c->n_active, k, T, H, I, c->h, c->hmax,
-                             max_active * (I / 8), c->err, c->sms, s));
-    }
-    {
-      Timed tm(c, MOE_K_DOWN, s);
-      CUDA_TRY(launch_gemv2(w2, s2, c->h, c->hmax, c->counts, c->offsets, c->active, c->n_active, T,
-                            H, I, c->y, max_active * (H / 16), c->err, c->sms, s));
-    }
   } else {
-    if (c->tm_w13_ptr != w13) {
-      if (!encode_u8_tmap(&c->tm_gemm1.b, w13, H, E * 2 * I, 64)) return MOE_ERR_CUDA;
-      c->tm_w13_ptr = w13;
+    if (path == MOE_PATH_GEMV) {
+      {
+        Timed tm(c, MOE_K_GATE_UP, s);
+        CUDA_TRY(launch_gemv13(w13, s13, c->x16, c->xscale, c->counts, c->offsets, c->perm,
+                               c->active, c->n_active, k, T, H, I, c->h, c->hmax,
+                               max_active * (I / 8), c->err, c->sms, s, slot_of));
+      }
+      {
+        Timed tm(c, MOE_K_DOWN, s);
+        CUDA_TRY(launch_gemv2(w2, s2, c->h, c->hmax, c->counts, c->offsets, c->active, c->n_active,
+                              T, H, I, c->y, max_active * (H / 16), c->err, c->sms, s, slot_of));
+      }
+    } else {
+      if (c->tm_w13_ptr != w13) {
+        if (!encode_u8_tmap(&c->tm_gemm1.b, w13, H, NS * 2 * I, 64)) return MOE_ERR_CUDA;
+        c->tm_w13_ptr = w13;
+      }
+      if (c->tm_w2_ptr != w2) {
+        if (!encode_u8_tmap(&c->tm_gemm2.b, w2, I, NS * H, 64)) return MOE_ERR_CUDA;
+        c->tm_w2_ptr = w2;
+      }
+      const int64_t max_tiles = (P + kTileM - 1) / kTileM + max_active;
+      {
+        Timed tm(c, MOE_K_ACT_QUANT, s);
+        CUDA_TRY(launch_act_quant(x, c->perm, P, k, H, Pm, c->a_hi, c->a_lo, c->a_scale, c->sms, s));
+      }
+      {
+        Timed tm(c, MOE_K_GATE_UP, s);
+        CUDA_TRY(launch_grouped_gemm(1, c->tm_gemm1, c->offsets, c->tile_offsets, c->a_scale, s13,
+                                     (int)E, H, I, Pm, c->h_t, c->h_scale, nullptr, c->err,
+                                     max_tiles * (I / 128), c->sms, s, slot_of));
+      }
+      {
+        Timed tm(c, MOE_K_DOWN, s);
+        CUDA_TRY(launch_grouped_gemm(2, c->tm_gemm2, c->offsets, c->tile_offsets, c->h_scale, s2,
+                                     (int)E, H, I, Pm, nullptr, nullptr, c->y, c->err,
+                                     max_tiles * (H / 256), c->sms, s, slot_of));
+      }
     }
-    if (c->tm_w2_ptr != w2) {
-      if (!encode_u8_tmap(&c->tm_gemm2.b, w2, I, E * H, 64)) return MOE_ERR_CUDA;
-      c->tm_w2_ptr = w2;
-    }
-    const int64_t max_tiles = (P + tile_m - 1) / tile_m + max_active;
     {
-      Timed tm(c, MOE_K_ACT_QUANT, s);
-      CUDA_TRY(launch_act_quant(x, c->perm, P, k, H, Pm, c->a_hi, c->a_lo, c->a_scale, c->sms, s));
+      Timed tm(c, MOE_K_COMBINE, s);
+      CUDA_TRY(launch_combine(c->y, 1, 0, c->inv, c->wts, T, k, H, out, s));
     }
-    {
-      Timed tm(c, MOE_K_GATE_UP, s);
-      CUDA_TRY(launch_grouped_gemm(1, c->tm_gemm1, c->offsets, c->tile_offsets, c->a_scale, s13,
-                                   (int)E, H, I, Pm, c->h_t, c->h_scale, nullptr, c->err,
-                                   max_tiles * (I / 128), c->sms, s));
-    }
-    {
-      Timed tm(c, MOE_K_DOWN, s);
-      CUDA_TRY(launch_grouped_gemm(2, c->tm_gemm2, c->offsets, c->tile_offsets, c->h_scale, s2,
-                                   (int)E, H, I, Pm, nullptr, nullptr, c->y, c->err,
-                                   max_tiles * (H / 256), c->sms, s));
-    }
-  }
-  {
-    Timed tm(c, MOE_K_COMBINE, s);
-    CUDA_TRY(launch_combine(c->y, 1, 0, c->inv, c->wts, T, k, H, out, s));
   }
   c->last_T = T;
   c->last_k = k;
   c->last_stream = s;
   if (c->timing && c->pending.size() > 16384) drain_timing(c);
   return MOE_OK;
+}
+
+int forward_device(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw,
+                   const float *rb, const uint8_t *w13, const float *s13, const uint8_t *w2,
+                   const float *s2, int k, __nv_bfloat16 *out, cudaStream_t s) {
+  const int path = resolve_path(c, T);
+  const int rc = route_phase(c, x, T, rw, rb, k, path, s);
+  if (rc != MOE_OK) return rc;
+  return expert_phase(c, x, T, w13, s13, w2, s2, k, path, out, s);
 }
 
 int check_forward_args(moe_ctx *c, const void *hidden, int64_t T, const float *rw,
@@ -356,6 +374,41 @@ int check_forward_args(moe_ctx *c, const void *hidden, int64_t T, const float *r
 }
 
 }  // namespace
+
+namespace fp8moe {
+
+int ctx_check_forward(moe_ctx *c, const void *hidden, int64_t T, const float *rw, const float *rb,
+                      const uint8_t *w13, const float *s13, const uint8_t *w2, const float *s2,
+                      int32_t k, const void *out, int *path) {
+  const int rc = check_forward_args(c, hidden, T, rw, rb, w13, s13, w2, s2, k, out);
+  if (rc == MOE_OK && path != nullptr) *path = resolve_path(c, T);
+  return rc;
+}
+
+int ctx_route(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw, const float *rb,
+              int k, int path, cudaStream_t s) {
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  return route_phase(c, x, T, rw, rb, k, path, s);
+}
+
+int ctx_experts(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const uint8_t *w13,
+                const float *s13, const uint8_t *w2, const float *s2, int k, int path,
+                __nv_bfloat16 *out, cudaStream_t s, const int32_t *slot_of, int64_t n_slabs) {
+  if (cudaSetDevice(c->cfg.device) != cudaSuccess) return MOE_ERR_CUDA;
+  return expert_phase(c, x, T, w13, s13, w2, s2, k, path, out, s, slot_of, n_slabs);
+}
+
+int ctx_active_experts(moe_ctx *c, int32_t *buf, cudaStream_t s) {
+  CUDA_TRY(cudaMemcpyAsync(buf, c->n_active, sizeof(int32_t), cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaMemcpyAsync(buf + 1, c->active, (size_t)c->cfg.n_experts * sizeof(int32_t),
+                           cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  return MOE_OK;
+}
+
+const moe_config *ctx_config(const moe_ctx *c) { return &c->cfg; }
+
+}  // namespace fp8moe
 
 extern "C" {
 

@@ -79,6 +79,7 @@ struct GemmArgs {
   float *h_scale;               //               power-of-two scales [I/128][Pmax]
   float *y;                     // GEMM2 output [Pmax, H]
   int *err;
+  const int32_t *slot_of;       // weight slab of each expert, or nullptr (slab = expert)
 };
 
 struct ItemCoords {
@@ -155,12 +156,13 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
       for (int64_t item = blockIdx.x; item < n_items && !abort_flag; item += gridDim.x) {
         const ItemCoords c = item_coords(p, item);
         int64_t b_rows[4];
+        const int64_t ws = p.slot_of ? __ldg(p.slot_of + c.e) : c.e;  // weight slab
         if (MODE == 1) {
-          const int64_t g = (int64_t)c.e * 2 * p.I + (int64_t)c.nb * 128;
+          const int64_t g = ws * 2 * p.I + (int64_t)c.nb * 128;
           const int64_t u = g + p.I;
           b_rows[0] = g; b_rows[1] = u; b_rows[2] = g + 64; b_rows[3] = u + 64;
         } else {
-          const int64_t r = (int64_t)c.e * p.H + (int64_t)c.nb * 256;
+          const int64_t r = ws * p.H + (int64_t)c.nb * 256;
           b_rows[0] = r; b_rows[1] = r + 64; b_rows[2] = r + 128; b_rows[3] = r + 192;
         }
         for (int64_t kb = 0; kb < nkb; ++kb) {
@@ -583,8 +585,9 @@ cudaError_t launch_grouped_gemm(int mode, const TmapSet &tm, const int32_t *offs
                                 const int32_t *tile_offsets, const float *a_scale,
                                 const float *w_scale, int E, int64_t H, int64_t I, int64_t Pmax,
                                 uint8_t *const h_terms[3], float *h_scale, float *y, int *err,
-                                int64_t max_items, int sms, cudaStream_t s) {
+                                int64_t max_items, int sms, cudaStream_t s, const int32_t *slot_of) {
   GemmArgs p;
+  p.slot_of = slot_of;
   p.offsets = offsets;
   p.tile_offsets = tile_offsets;
   p.a_scale = a_scale;

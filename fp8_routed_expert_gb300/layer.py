@@ -175,3 +175,70 @@ class MoELayer:
         if cap > n.value:
             raise ValueError(f"buffer {name!r} holds {n.value} bytes, asked for {cap}")
         return out
+
+
+CACHE_STATS = ("hits", "misses", "prefetched", "prefetch_used", "evictions", "bytes_copied")
+
+
+class ExpertCache:
+    """Experts kept in host memory with ``n_slots`` of them cached in device
+    memory (see moe_cache_init in include/fp8moe.h).  ``w13_host`` /
+    ``w2_host``: CPU uint8 tensors [E, 2I, H] / [E, H, I] that must stay alive
+    and unchanged while the cache exists."""
+
+    def __init__(self, layer: MoELayer, w13_host: torch.Tensor, w2_host: torch.Tensor, n_slots: int):
+        c = layer.cfg
+        E, H, I = c.n_experts, c.hidden, c.inter
+        for t, shape in ((w13_host, (E, 2 * I, H)), (w2_host, (E, H, I))):
+            if t.is_cuda or t.dtype != torch.uint8 or tuple(t.shape) != shape or not t.is_contiguous():
+                raise ValueError(f"expected a contiguous CPU uint8 tensor {shape}")
+        self.layer, self._keep = layer, (w13_host, w2_host)
+        h = ctypes.c_void_p()
+        check(lib().moe_cache_init(ctypes.byref(h), layer.handle, _ptr(w13_host), _ptr(w2_host),
+                                   n_slots), "moe_cache_init")
+        self._h = h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None) is not None and self._h.value:
+            lib().moe_cache_free(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def forward(self, x: torch.Tensor, router_w, router_bias, s13, s2, top_k: int,
+                out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty_like(x)
+        rc = lib().moe_cache_forward(self._h, _ptr(x), x.shape[0], _ptr(router_w), _ptr(router_bias),
+                                     _ptr(s13), _ptr(s2), top_k, _ptr(out), _stream_handle(stream))
+        check(rc, "moe_cache_forward")
+        return out
+
+    def guess(self, x: torch.Tensor, router_w, router_bias, top_k: int, n_guess: int) -> list:
+        buf = (ctypes.c_int32 * max(n_guess, 1))()
+        n = lib().moe_cache_guess(self._h, _ptr(x), x.shape[0], _ptr(router_w), _ptr(router_bias),
+                                  top_k, n_guess, buf)
+        if n < 0:
+            check(n, "moe_cache_guess")
+        return list(buf[:n])
+
+    def prefetch(self, experts) -> int:
+        arr = (ctypes.c_int32 * max(len(experts), 1))(*experts)
+        n = lib().moe_cache_prefetch(self._h, arr, len(experts))
+        if n < 0:
+            check(n, "moe_cache_prefetch")
+        return n
+
+    def stats(self) -> dict:
+        buf = (ctypes.c_int64 * len(CACHE_STATS))()
+        check(lib().moe_cache_stats(self._h, buf, len(CACHE_STATS)), "moe_cache_stats")
+        return dict(zip(CACHE_STATS, buf))
+
+    def resident(self) -> list:
+        buf = (ctypes.c_int32 * self.layer.cfg.n_experts)()
+        check(lib().moe_cache_resident(self._h, buf), "moe_cache_resident")
+        return list(buf)

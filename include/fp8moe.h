@@ -221,6 +221,85 @@ int moe_debug_copy(moe_ctx *ctx, const char *name, void *dst, int64_t capacity, 
                    void *stream);
 
 /*
+ * Experts larger than device memory (DeepSeek-V4.1-Flash post, "Bytes per
+ * token decide everything" and "Making it faster", v4: a cache in front of
+ * the slow tier and the next layer's experts guessed from its router and
+ * prefetched into the gap; Qwen post, "Where the time actually goes":
+ * speculative copies one layer early).  The expert weights (e4m3 codes) stay
+ * in host memory; `n_slots` experts at a time are held in device memory
+ * (slabs of one expert's W13 and W2 codes) and streamed in over NVLink-C2C;
+ * the layer's own kernels read expert e's codes from the slab a table names.
+ * The f32 block scales (1/16384 of the codes) stay resident and are passed
+ * as device pointers.
+ *
+ * moe_cache_init - create a cache for context `ctx`.
+ *   w13_host : host, e4m3 [E, 2I, H] (layout of moe_layer_forward's w13).
+ *   w2_host  : host, e4m3 [E, H, I].
+ *   n_slots  : experts held in device memory, 1..E (3*I*H bytes of device
+ *              memory each).
+ * The host ranges are page-locked (cudaHostRegister) for the life of the
+ * cache unless the caller already registered them; they must stay valid and
+ * unchanged until moe_cache_free.
+ * Errors: MOE_ERR_ARG, MOE_ERR_SHAPE (n_slots out of range), MOE_ERR_NOMEM,
+ * MOE_ERR_CUDA.
+ */
+typedef struct moe_expert_cache moe_expert_cache;
+int moe_cache_init(moe_expert_cache **out, moe_ctx *ctx, const uint8_t *w13_host,
+                   const uint8_t *w2_host, int64_t n_slots);
+
+/*
+ * moe_cache_forward - moe_layer_forward with the cache's experts: routes on
+ * `stream`, waits for the active-expert list (a host synchronisation of
+ * `stream`), brings the missing experts into least recently used slots
+ * (copies on `stream`), waits for earlier prefetches, then enqueues the
+ * expert kernels and the combine.  Results are bit-identical to
+ * moe_layer_forward with the same weights in device memory.  Consecutive
+ * forwards of one cache must use one stream.  MOE_ERR_NOMEM if the batch
+ * needs more experts than there are slots.
+ */
+int moe_cache_forward(moe_expert_cache *c, const void *hidden, int64_t T, const float *router_w,
+                      const float *router_bias, const float *s13, const float *s2, int32_t top_k,
+                      void *out, void *stream);
+
+/*
+ * moe_cache_prefetch - start bringing `experts` (host array of n expert
+ * ids, best guess first) into the cache on the cache's own copy stream,
+ * into slots that the last forward does not use; stops when no such slot is
+ * left.  Returns the number of copies started (>= 0) or an error.  The next
+ * moe_cache_forward waits for them.
+ */
+int moe_cache_prefetch(moe_expert_cache *c, const int32_t *experts, int64_t n);
+
+/*
+ * moe_cache_guess - the experts a router would pick for `hidden`: routes
+ * hidden (device bf16 [T, H], T <= 64) with router_w / router_bias (device,
+ * f32 [E, H] / [E] or NULL) on the cache's own stream, and writes to
+ * experts_out (host, n_guess ints) the chosen experts ordered by the number
+ * of tokens choosing them, then by their best rank, then by id.  Used with
+ * the NEXT layer's router on this layer's input to guess what to prefetch.
+ * Returns the number written (<= n_guess) or an error.
+ */
+int moe_cache_guess(moe_expert_cache *c, const void *hidden, int64_t T, const float *router_w,
+                    const float *router_bias, int32_t top_k, int32_t n_guess, int32_t *experts_out);
+
+/* moe_cache_stats - counters since moe_cache_init, out[0 .. n-1] (host). */
+#define MOE_CACHE_HITS 0          /* active experts found in the cache        */
+#define MOE_CACHE_MISSES 1        /* active experts copied in by a forward    */
+#define MOE_CACHE_PREFETCHED 2    /* experts copied in by moe_cache_prefetch  */
+#define MOE_CACHE_PREFETCH_USED 3 /* prefetched experts a forward then used   */
+#define MOE_CACHE_EVICTIONS 4
+#define MOE_CACHE_BYTES_COPIED 5  /* host -> device bytes of expert codes     */
+#define MOE_CACHE_STATS 6
+int moe_cache_stats(const moe_expert_cache *c, int64_t *out, int32_t n);
+
+/* moe_cache_resident - slot of every expert, -1 if not cached (host int[E]). */
+int moe_cache_resident(const moe_expert_cache *c, int32_t *slot_of_expert);
+
+/* moe_cache_free - wait for the device and release everything; NULL is a
+ * no-op. */
+void moe_cache_free(moe_expert_cache *c);
+
+/*
  * moe_selftest_wait_timeout - exercise the bounded device-side waits.  Every
  * wait inside the layer's kernels (mbarriers of TMA copies and tensor-core
  * work, cross-CTA counters) gives up after a time limit and records

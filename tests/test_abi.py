@@ -56,6 +56,14 @@ def test_null_arguments(L):
     assert L.moe_set_path(None, 0) == moe.C["MOE_ERR_ARG"]
     assert L.moe_resolve_path(None, 1) == moe.C["MOE_ERR_ARG"]
     assert L.moe_selftest_wait_timeout(None, 1000, None, None) == moe.C["MOE_ERR_ARG"]
+    assert L.moe_cache_init(None, None, None, None, 1) == moe.C["MOE_ERR_ARG"]
+    h = ctypes.c_void_p(99)
+    assert L.moe_cache_init(ctypes.byref(h), None, None, None, 1) == moe.C["MOE_ERR_ARG"]
+    assert h.value is None
+    assert L.moe_cache_forward(None, None, 1, None, None, None, None, 1, None, None) == moe.C["MOE_ERR_ARG"]
+    assert L.moe_cache_prefetch(None, None, 0) == moe.C["MOE_ERR_ARG"]
+    assert L.moe_cache_stats(None, None, 0) == moe.C["MOE_ERR_ARG"]
+    L.moe_cache_free(None)
 
 
 def test_error_strings(L):
