@@ -558,7 +558,10 @@ def run_stream(args) -> dict:
         w = W.make_weights(f)
         layers.append(dict(
             rw=g(w.router_w), rb=None if w.router_bias is None else g(w.router_bias),
-            s13=g(w.s13), s2=g(w.s2), w13_host=torch.from_numpy(w.w13), w2_host=torch.from_numpy(w.w2),
+            s13=g(w.s13), s2=g(w.s2),
+            # page-locked buffers allocated by the CUDA driver (placed for the
+            # GPU's host link), as an engine loading the experts would use
+            w13_host=torch.from_numpy(w.w13).pin_memory(), w2_host=torch.from_numpy(w.w2).pin_memory(),
             w13=g(w.w13), w2=g(w.w2),
             ctx=MoELayer(T, fam.hidden, fam.n_experts, fam.inter, k, 0)))
     for ly in layers:

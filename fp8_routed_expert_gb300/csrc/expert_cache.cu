@@ -167,11 +167,19 @@ int moe_cache_init(moe_expert_cache **out, moe_ctx *ctx, const uint8_t *w13_host
     Matrix &mx = c->m[i];
     const size_t total = (size_t)E * mx.bytes;
     // page-locked host memory lets the copies run asynchronously at full
-    // link speed; memory the caller already registered is used as it is
-    const cudaError_t er = cudaHostRegister(const_cast<uint8_t *>(mx.host), total, cudaHostRegisterDefault);
-    if (er == cudaSuccess) mx.registered = true;
-    else if (er == cudaErrorHostMemoryAlreadyRegistered) cudaGetLastError();
-    else { cudaGetLastError(); rc = MOE_ERR_CUDA; break; }
+    // link speed; memory that already is page-locked (cudaHostAlloc or an
+    // earlier registration) is used as it is
+    cudaPointerAttributes pa;
+    const bool locked = cudaPointerGetAttributes(&pa, mx.host) == cudaSuccess &&
+                        pa.type == cudaMemoryTypeHost;
+    cudaGetLastError();
+    if (!locked) {
+      const cudaError_t er =
+          cudaHostRegister(const_cast<uint8_t *>(mx.host), total, cudaHostRegisterDefault);
+      if (er == cudaSuccess) mx.registered = true;
+      else if (er == cudaErrorHostMemoryAlreadyRegistered) cudaGetLastError();
+      else { cudaGetLastError(); rc = MOE_ERR_CUDA; break; }
+    }
     if (cudaMalloc(&mx.slabs, (size_t)n_slots * mx.bytes) != cudaSuccess) {
       cudaGetLastError();
       mx.slabs = nullptr;
