@@ -37,7 +37,7 @@ def exported_functions() -> list[str]:
     """Names of the functions the header declares."""
     src = open(HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:int|void|const char \*)\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|int64_t|void|const char \*)\s*\*?\s*(moe_\w+)\s*\(", src, flags=re.M)))
 
 
 def lib():
@@ -74,6 +74,10 @@ def lib():
         "moe_cache_stats": ([vp, vp, i32], ctypes.c_int),
         "moe_cache_resident": ([vp, vp], ctypes.c_int),
         "moe_cache_free": ([vp], None),
+        "moe_set_sm_budget": ([vp, i32], ctypes.c_int),
+        "moe_attention_workspace_bytes": ([i64, i64, i32, i32], i64),
+        "moe_decode_attention": ([vp, vp, vp, i64, i64, i32, i32, i32, vp, vp, i64, vp],
+                                 ctypes.c_int),
         "moe_route_noalloc": ([vp, i64, i64, vp, vp, i64, i32, vp, vp, vp, vp, vp, vp, vp],
                               ctypes.c_int),
         "moe_debug_copy": ([vp, ctypes.c_char_p, vp, i64, ctypes.POINTER(ctypes.c_int64), vp],

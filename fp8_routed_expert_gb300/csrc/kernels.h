@@ -170,6 +170,15 @@ cudaError_t launch_fp4_down(const uint8_t *w2, const uint8_t *sf2, const float *
                             const int32_t *active, const int32_t *n_active, int64_t T, int64_t H,
                             int64_t I, float *y, int64_t max_items, int sms, cudaStream_t s);
 
+// Decode attention (sub-block-1 of a shortcut-connected MoE layer): q bf16
+// [B, n_heads, 128], K / V caches bf16 [B, S, n_kv_heads, 128], o bf16
+// [B, n_heads, 128]; part: f32 workspace of B * n_heads * attention_chunks(S)
+// * 130 floats.  n_heads / n_kv_heads in {1, 2, 4, 8}.
+int64_t attention_chunks(int64_t S);
+cudaError_t launch_decode_attention(const __nv_bfloat16 *q, const __nv_bfloat16 *kc,
+                                    const __nv_bfloat16 *vc, int64_t B, int64_t S, int nh, int nkv,
+                                    int d, float *part, __nv_bfloat16 *o, cudaStream_t s);
+
 // One CTA whose waits (an mbarrier nothing arrives on, a global counter
 // nothing increments) run out after limit_ns each: records DEV_ERR_TIMEOUT in
 // *err and, if `which` is given, which waits gave up (bit 0 the mbarrier,

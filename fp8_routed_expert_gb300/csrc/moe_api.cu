@@ -26,7 +26,8 @@ struct TimingRec {
 
 struct moe_ctx {
   moe_config cfg{};
-  int sms = 0;
+  int sms = 0;        // SMs the persistent kernels may use (moe_set_sm_budget)
+  int sms_total = 0;  // SMs of the device
   char *ws = nullptr;
   size_t ws_bytes = 0;
   // workspace views
@@ -454,6 +455,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
   if (c == nullptr) return MOE_ERR_NOMEM;
   c->cfg = *cfg;
   c->sms = prop.multiProcessorCount;
+  c->sms_total = prop.multiProcessorCount;
 
   const int64_t Tm = cfg->max_tokens, E = cfg->n_experts, H = cfg->hidden, I = cfg->inter;
   const int64_t Pm = Tm * cfg->max_top_k;
@@ -636,6 +638,40 @@ int moe_selftest_wait_timeout(moe_ctx *c, int64_t limit_ns, int32_t *which, void
   c->n_launches += 1;
   CUDA_TRY(launch_bounded_wait_selftest(c->idle, (uint64_t)limit_ns, c->err, which, s));
   c->last_stream = s;
+  return MOE_OK;
+}
+
+int moe_set_sm_budget(moe_ctx *c, int32_t n_sms) {
+  if (c == nullptr) return MOE_ERR_ARG;
+  c->sms = (n_sms <= 0 || n_sms > c->sms_total) ? c->sms_total : n_sms;
+  return MOE_OK;
+}
+
+int64_t moe_attention_workspace_bytes(int64_t B, int64_t S, int32_t n_heads, int32_t head_dim) {
+  if (B < 0 || S < 1 || n_heads < 1 || head_dim < 1) return MOE_ERR_ARG;
+  return B * n_heads * attention_chunks(S) * (head_dim + 2) * (int64_t)sizeof(float);
+}
+
+int moe_decode_attention(const void *q, const void *k_cache, const void *v_cache, int64_t B,
+                         int64_t S, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, void *out,
+                         void *workspace, int64_t workspace_bytes, void *stream) {
+  if (B < 0 || S < 1) return MOE_ERR_ARG;
+  if (head_dim != 128 || n_kv_heads < 1 || n_heads < n_kv_heads || n_heads % n_kv_heads != 0)
+    return MOE_ERR_SHAPE;
+  const int g = n_heads / n_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return MOE_ERR_SHAPE;
+  if (B > 65535 || n_kv_heads > 65535 || attention_chunks(S) > INT32_MAX) return MOE_ERR_SHAPE;
+  if (B == 0) return MOE_OK;
+  if (!q || !k_cache || !v_cache || !out || !workspace) return MOE_ERR_ARG;
+  if (workspace_bytes < moe_attention_workspace_bytes(B, S, n_heads, head_dim)) return MOE_ERR_ARG;
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+      !aligned(workspace, 16))
+    return MOE_ERR_ALIGN;
+  CUDA_TRY(launch_decode_attention(static_cast<const __nv_bfloat16 *>(q),
+                                   static_cast<const __nv_bfloat16 *>(k_cache),
+                                   static_cast<const __nv_bfloat16 *>(v_cache), B, S, n_heads,
+                                   n_kv_heads, head_dim, static_cast<float *>(workspace),
+                                   static_cast<__nv_bfloat16 *>(out), static_cast<cudaStream_t>(stream)));
   return MOE_OK;
 }
 

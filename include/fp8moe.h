@@ -300,6 +300,39 @@ int moe_cache_resident(const moe_expert_cache *c, int32_t *slot_of_expert);
 void moe_cache_free(moe_expert_cache *c);
 
 /*
+ * Shortcut-connected MoE (dragon.c, "Shortcut-connected MoE": the MoE is
+ * computed on sub-block-0's normed hidden state and its output is added at
+ * the END of sub-block-1, "a designed overlap window"; §10: "thread the MoE
+ * against sub-block-1's attention").  The MoE forward and sub-block-1's
+ * attention run on two streams; the two calls below make that overlap work.
+ *
+ * moe_set_sm_budget - let the layer's persistent kernels (one CTA per SM)
+ * use at most n_sms SMs, leaving the rest to work on other streams; n_sms
+ * <= 0 restores all SMs.  Takes effect from the next forward.
+ */
+int moe_set_sm_budget(moe_ctx *ctx, int32_t n_sms);
+
+/*
+ * moe_decode_attention - softmax attention of one new token per sequence
+ * against its key/value cache:
+ *   out[b, h] = softmax(q[b, h] . K[b, :, c]^T / sqrt(d)) V[b, :, c],
+ *   c = h / (n_heads / n_kv_heads).
+ *   q        : device bf16 [B, n_heads, d];
+ *   k_cache, v_cache : device bf16 [B, S, n_kv_heads, d];
+ *   out      : device bf16 [B, n_heads, d];
+ *   workspace: device, at least moe_attention_workspace_bytes(B, S,
+ *              n_heads, d) bytes (f32 partial results; caller-owned).
+ * d must be 128; n_heads / n_kv_heads one of 1, 2, 4, 8 (MOE_ERR_SHAPE
+ * otherwise); pointers 16-byte aligned.  f32 arithmetic, bf16 output.  No
+ * counterpart in the pages beyond its role: sub-block-1's attention, the
+ * work the MoE overlaps.
+ */
+int64_t moe_attention_workspace_bytes(int64_t B, int64_t S, int32_t n_heads, int32_t head_dim);
+int moe_decode_attention(const void *q, const void *k_cache, const void *v_cache, int64_t B,
+                         int64_t S, int32_t n_heads, int32_t n_kv_heads, int32_t head_dim, void *out,
+                         void *workspace, int64_t workspace_bytes, void *stream);
+
+/*
  * moe_selftest_wait_timeout - exercise the bounded device-side waits.  Every
  * wait inside the layer's kernels (mbarriers of TMA copies and tensor-core
  * work, cross-CTA counters) gives up after a time limit and records
