@@ -78,6 +78,10 @@ def parse():
     ap.add_argument("--guesses", type=int, default=0,
                     help="experts of the next layer to prefetch, guessed with its router on "
                          "this layer's input (default: top_k)")
+    ap.add_argument("--scmoe", action="store_true",
+                    help="time the MoE beside sub-block-1's decode attention (shortcut-connected "
+                         "MoE): alone, one after the other, and concurrently on two streams")
+    ap.add_argument("--context", type=int, default=4096, help="--scmoe: keys per sequence")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     return ap.parse_args()
@@ -624,6 +628,132 @@ def run_stream(args) -> dict:
     }
 
 
+def run_scmoe(args) -> dict:
+    """Shortcut-connected MoE overlap.  The MoE runs on sub-block-0's output
+    while sub-block-1's attention (one new token per sequence over a cache of
+    --context keys, heads = H / 128) runs on another stream; the MoE's
+    persistent kernels get an SM budget so that the attention finds free SMs.
+    Reported: each alone, one after the other, and overlapped (best budget)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from fp8_routed_expert_gb300 import MoELayer, lib
+
+    fam, T = W.parse_workload(args.workload)
+    k, S = fam.top_k, args.context
+    nh = fam.hidden // 128
+    dev = torch.device("cuda", 0)
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    bf = lambda bits: torch.from_numpy(bits.astype(np.int16)).view(torch.bfloat16).to(dev)
+    w = W.make_weights(fam)
+    rw, rb = g(w.router_w), (None if w.router_bias is None else g(w.router_bias))
+    w13, s13, w2, s2 = g(w.w13), g(w.s13), g(w.w2), g(w.s2)
+    x = bf(W.make_x(fam, T))
+    q = bf(W.normal_bf16(77, 11, (T, nh, 128)))
+    kc = bf(W.normal_bf16(77, 12, (T, S, nh, 128)))
+    vc = bf(W.normal_bf16(77, 13, (T, S, nh, 128)))
+    att = torch.empty_like(q)
+    ws = torch.empty(lib().moe_attention_workspace_bytes(T, S, nh, 128), dtype=torch.uint8, device=dev)
+    moe_out = torch.empty_like(x)
+    layer = MoELayer(T, fam.hidden, fam.n_experts, fam.inter, k, 0)
+    # the MoE's stream has the higher priority: its short routing kernels and
+    # its expert kernels are scheduled ahead of waiting attention CTAs
+    lo, hi = torch.cuda.Stream.priority_range() if hasattr(torch.cuda.Stream, "priority_range") \
+        else (0, -1)
+    sa, sb = torch.cuda.Stream(dev, priority=hi), torch.cuda.Stream(dev, priority=lo)
+    flush_w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def moe(st):
+        layer.forward(x, rw, rb, w13, s13, w2, s2, k, out=moe_out, stream=st)
+
+    def attn(st):
+        rc = lib().moe_decode_attention(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), T, S, nh, nh, 128,
+                                        att.data_ptr(), ws.data_ptr(), ws.numel(), st.cuda_stream)
+        assert rc == 0
+
+    def timed(fn, reps):
+        ms = []
+        for _ in range(reps):
+            flush_w.zero_()
+            torch.cuda.synchronize(dev)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(sa)
+            fn()
+            ev = torch.cuda.Event()
+            ev.record(sb)
+            sa.wait_event(ev)
+            b.record(sa)
+            b.synchronize()
+            ms.append(a.elapsed_time(b))
+        return statistics.median(ms) * 1e3
+
+    def serial():
+        moe(sa)
+        attn(sa)
+
+    def overlapped():
+        ev = torch.cuda.Event()
+        ev.record(sa)
+        sb.wait_event(ev)
+        moe(sa)
+        attn(sb)
+
+    reps = max(args.steps, 20)
+    for fn in (lambda: moe(sa), lambda: attn(sa), serial, overlapped):
+        timed(fn, 3)
+    # the same with the experts streamed from host memory through an expert
+    # cache: the copies of missing experts (copy engine, no SMs) can run
+    # under the attention -- the pages' point of the overlap window
+    from fp8_routed_expert_gb300 import ExpertCache
+    slots = args.expert_cache or min(fam.n_experts, 48)
+    cache = ExpertCache(layer, torch.from_numpy(w.w13).pin_memory(), torch.from_numpy(w.w2).pin_memory(),
+                        slots)
+    xs = [bf(W.normal_bf16(9500 + i, W.configs.TID_X, (T, fam.hidden))) for i in range(4 * reps + 40)]
+    it = iter(xs)
+
+    def moe_cached(st):
+        cache.forward(next(it), rw, rb, s13, s2, k, out=moe_out, stream=st)
+
+    def serial_cached():
+        attn(sa)
+        moe_cached(sa)
+
+    def overlapped_cached():
+        ev = torch.cuda.Event()
+        ev.record(sa)
+        sb.wait_event(ev)
+        attn(sb)          # enqueued first: runs while the MoE routes and copies
+        moe_cached(sa)
+
+    for fn in (lambda: moe_cached(sa), serial_cached, overlapped_cached):
+        timed(fn, 3)
+    cached = {"slots": slots, "moe_us": timed(lambda: moe_cached(sa), reps),
+              "serial_us": timed(serial_cached, reps), "overlapped_us": timed(overlapped_cached, reps)}
+    cached["saved_frac"] = 1 - cached["overlapped_us"] / cached["serial_us"]
+    cache.close()
+    res = {"moe_us": timed(lambda: moe(sa), reps), "attention_us": timed(lambda: attn(sa), reps),
+           "serial_us": timed(serial, reps)}
+    budgets = {}
+    for budget in (0, 136, 120, 104, 88):
+        lib().moe_set_sm_budget(layer.handle, budget)
+        timed(overlapped, 3)
+        budgets[str(budget or "all")] = timed(overlapped, reps)
+    lib().moe_set_sm_budget(layer.handle, 0)
+    best = min(budgets, key=budgets.get)
+    res.update(overlapped_us_by_moe_sm_budget=budgets, best_budget=best,
+               overlapped_us=budgets[best], saved_frac=1 - budgets[best] / res["serial_us"],
+               streamed_experts=cached)
+    kv_bytes = 2 * T * S * nh * 128 * 2
+    return {"metric": METRIC, "value": T / (budgets[best] / 1e6), "unit": UNIT, "n_gpus": 1,
+            "steps": reps, "warmup": 3, "ms_per_step": budgets[best] / 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 weights x multi-term e4m3 activations, f32 accumulate; bf16 attention",
+            "data": "synthetic", "config": {"workload": f"{args.workload} beside decode attention",
+                                             "context": S, "heads": nh, "kv_bytes": kv_bytes,
+                                             "l2": "flushed before every rep"},
+            "scmoe": res}
+
+
 def main():
     args = parse()
     rank, local_rank, world = dist_env()
@@ -638,6 +768,10 @@ def main():
         print(json.dumps(r))
         return 0
 
+    if args.scmoe:
+        args.steps = args.steps or 50
+        print(json.dumps(run_scmoe(args)))
+        return 0
     if args.expert_cache:
         args.steps = args.steps or 50
         args.warmup = max(args.warmup or 5, 3)

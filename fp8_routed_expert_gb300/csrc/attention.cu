@@ -21,7 +21,7 @@ namespace {
 
 constexpr int kAttD = 128;        // head dimension
 constexpr int kAttChunk = 256;    // keys per CTA
-constexpr int kAttThreads = 128;  // one thread per output column in the P.V phase
+constexpr int kAttThreads = 128;  // threads per CTA
 constexpr int kAttMaxG = 8;       // query heads per key/value head
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &v, float (&f)[8]) {
@@ -39,7 +39,9 @@ __global__ void __launch_bounds__(kAttThreads) attn_chunk_kernel(
     const __nv_bfloat16 *__restrict__ vc, int64_t S, int nh, int nkv, float scale,
     float *__restrict__ part, int n_chunks) {
   __shared__ float qs[G][kAttD];
-  __shared__ float ps[G][kAttChunk];
+  // scores / weights of the chunk; reused afterwards for the four warps'
+  // partial outputs, [4][G][128] floats, twice the scores' size
+  __shared__ float ps[G][2 * kAttChunk];
   __shared__ float red[G][kAttThreads / 32];
   const int t = threadIdx.x, lane = t & 31, wid = t >> 5;
   const int chunk = blockIdx.x, c = blockIdx.y;
@@ -64,7 +66,7 @@ __global__ void __launch_bounds__(kAttThreads) attn_chunk_kernel(
     for (int h = 0; h < G; ++h) s[h] = 0.f;
     if (jj < nk) {
       const uint4 *kr = reinterpret_cast<const uint4 *>(kc + ((b * S + j0 + jj) * nkv + c) * kAttD);
-#pragma unroll 4
+#pragma unroll 8
       for (int v8 = 0; v8 < kAttD / 8; ++v8) {
         float kf[8];
         bf16x8_to_f32(__ldg(kr + v8), kf);
@@ -113,23 +115,48 @@ __global__ void __launch_bounds__(kAttThreads) attn_chunk_kernel(
     if (lane == 0) red[h][wid] = l;
   }
   __syncthreads();
-  // ---- P.V: thread t owns output column t of every head
-  float acc[G];
+  // ---- P.V: thread t takes columns 8 (t % 16) .. + 7 of keys t / 16,
+  // t / 16 + 8, ..: one 16-byte load per key, 8 keys per 128 threads
+  const int cg = t & 15, kl = t >> 4;
+  float acc[G][8];
 #pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = 0.f;
-  const __nv_bfloat16 *vcol = vc + ((b * S + j0) * nkv + c) * kAttD + t;
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[h][i] = 0.f;
   const int64_t vstride = (int64_t)nkv * kAttD;
-#pragma unroll 8
-  for (int jj = 0; jj < nk; ++jj) {
-    const float v = __bfloat162float(vcol[jj * vstride]);
+  const __nv_bfloat16 *vrow = vc + ((b * S + j0) * nkv + c) * kAttD + 8 * cg;
+#pragma unroll 4
+  for (int jj = kl; jj < nk; jj += 8) {
+    float vf[8];
+    bf16x8_to_f32(__ldg(reinterpret_cast<const uint4 *>(vrow + jj * vstride)), vf);
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = fmaf(ps[h][jj], v, acc[h]);
+    for (int h = 0; h < G; ++h) {
+      const float pj = ps[h][jj];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(pj, vf[i], acc[h][i]);
+    }
   }
+  // sum over the 8 key lanes: the two of a warp by a shuffle, then the four
+  // warps through shared memory (the scores are no longer needed)
+  float *accs = &ps[0][0];  // [4 warps][G][128] = G * 2 * kAttChunk floats
+  static_assert((kAttThreads / 32) * kAttD == 2 * kAttChunk, "partials fit the score buffer");
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float v = acc[h][i] + __shfl_xor_sync(0xffffffffu, acc[h][i], 16);
+      if ((lane >> 4) == 0) accs[(wid * G + h) * kAttD + 8 * cg + i] = v;
+    }
+  __syncthreads();
   // partial layout [b][head][chunk][d + 2]: acc, then m and l
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     float *pp = part + (((b * nh + (int64_t)c * G + h) * n_chunks) + chunk) * (kAttD + 2);
-    pp[t] = acc[h];
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < kAttThreads / 32; ++w) a += accs[(w * G + h) * kAttD + t];
+    pp[t] = a;
     if (t == 0) {
       float l = 0.f;
       for (int w = 0; w < kAttThreads / 32; ++w) l += red[h][w];
