@@ -93,6 +93,7 @@ cudaError_t launch_act_quant(const __nv_bfloat16 *x, const int32_t *perm, int64_
 // boxes of 32 rows x 32 columns, 128-byte swizzle).
 struct TmapSet {
   CUtensorMap a[3];
+  CUtensorMap a64[3];  // the same activation terms in boxes of 64 rows (half tiles)
   CUtensorMap b;
   CUtensorMap st[3];
 };

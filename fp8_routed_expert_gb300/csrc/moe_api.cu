@@ -520,6 +520,12 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       !encode_u8_tmap(&c->tm_gemm2.a[0], c->h_t[0], I, Pr, 128) ||
       !encode_u8_tmap(&c->tm_gemm2.a[1], c->h_t[1], I, Pr, 128) ||
       !encode_u8_tmap(&c->tm_gemm2.a[2], c->h_t[2], I, Pr, 128) ||
+      !encode_u8_tmap(&c->tm_gemm1.a64[0], c->a_hi, H, Pr, 64) ||
+      !encode_u8_tmap(&c->tm_gemm1.a64[1], c->a_lo, H, Pr, 64) ||
+      !encode_u8_tmap(&c->tm_gemm1.a64[2], c->a_lo, H, Pr, 64) ||
+      !encode_u8_tmap(&c->tm_gemm2.a64[0], c->h_t[0], I, Pr, 64) ||
+      !encode_u8_tmap(&c->tm_gemm2.a64[1], c->h_t[1], I, Pr, 64) ||
+      !encode_u8_tmap(&c->tm_gemm2.a64[2], c->h_t[2], I, Pr, 64) ||
       !encode_h_store_tmap(&c->tm_gemm1.st[0], c->h_t[0], I, Pr) ||
       !encode_h_store_tmap(&c->tm_gemm1.st[1], c->h_t[1], I, Pr) ||
       !encode_h_store_tmap(&c->tm_gemm1.st[2], c->h_t[2], I, Pr) ||

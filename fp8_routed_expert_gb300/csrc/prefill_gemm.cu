@@ -24,7 +24,11 @@
 // the per-128-column scale folding of dragon.c §8 "Round 3", done per K block
 // in f32.
 //
-// Tile: 128 rows (positions of one expert's segment) x 256 columns x K.
+// Tile: 128 rows (positions of one expert's segment) x 256 columns x K.  A
+// tile with at most 64 rows in the segment (most experts of a large, skewed
+// batch hold only a few dozen positions) loads 64 activation rows and runs
+// M = 64 MMAs, half the tensor work; its accumulator rows then sit in TMEM
+// lanes 32 q + l, l < 16 (row 16 q + l), so each epilogue warp holds 16 rows.
 //   GEMM1 (gate/up): the 256 B rows are gate rows [n0, n0+64), up rows
 //   [I+n0, I+n0+64), gate rows [n0+64, n0+128), up rows [I+n0+64, I+n0+128)
 //   with n0 = 128 nb, so each epilogue warp holds the gate and up values of
@@ -135,7 +139,10 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
     }
     abort_flag = 0;
     fence_mbar_init();
-    for (int t = 0; t < NT; ++t) prefetch_tmap(&tm.a[t]);
+    for (int t = 0; t < NT; ++t) {
+      prefetch_tmap(&tm.a[t]);
+      prefetch_tmap(&tm.a64[t]);
+    }
     prefetch_tmap(&tm.b);
     for (int t = 0; t < (MODE == 1 ? 3 : 1); ++t) prefetch_tmap(&tm.st[t]);
   }
@@ -165,17 +172,19 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
           const int64_t r = ws * p.H + (int64_t)c.nb * 256;
           b_rows[0] = r; b_rows[1] = r + 64; b_rows[2] = r + 128; b_rows[3] = r + 192;
         }
+        const bool half_m = c.row_end - c.m0 <= 64;  // M = 64 item: 64 activation rows
         for (int64_t kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag, WAIT_LIMIT_NS)) {
             raise_abort(&abort_flag, p.err);
             break;
           }
           uint8_t *sa = smem + (size_t)stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+          mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES - (half_m ? NT * A_TILE / 2 : 0));
           const int32_t kx = (int32_t)(kb * BK);
 #pragma unroll
           for (int t = 0; t < NT; ++t)
-            tma_load_2d(sa + t * A_TILE, &tm.a[t], kx, (int32_t)c.m0, &full_bar[stage]);
+            tma_load_2d(sa + t * A_TILE, half_m ? &tm.a64[t] : &tm.a[t], kx, (int32_t)c.m0,
+                        &full_bar[stage]);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             tma_load_2d(sa + NT * A_TILE + q * (B_BOX_ROWS * BK), &tm.b, kx, (int32_t)b_rows[q],
@@ -187,10 +196,12 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_e4m3_f32(BM, BN);
+      const uint32_t idesc128 = idesc_e4m3_f32(BM, BN), idesc64 = idesc_e4m3_f32(64, BN);
       int stage = 0, buf = 0;
       uint32_t phase = 0, bphase = 0;
       for (int64_t item = blockIdx.x; item < n_items && !abort_flag; item += gridDim.x) {
+        const ItemCoords c = item_coords(p, item);
+        const uint32_t idesc = c.row_end - c.m0 <= 64 ? idesc64 : idesc128;
         for (int64_t kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&tempty_bar[buf], bphase ^ 1u, &abort_flag, WAIT_LIMIT_NS) ||
               !mbar_wait(&full_bar[stage], phase, &abort_flag, WAIT_LIMIT_NS)) {
@@ -222,13 +233,16 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
     const int quarter = warp & 3;             // TMEM lanes this warp may read
     const int half = (warp - 2) >> 2;         // column half of the 256-wide tile
     uint8_t *stg_warp = smem + (size_t)STAGES * STAGE_BYTES + (size_t)(warp - 2) * Pipe<NT>::STG_WARP;
-    const int r_in_tile = quarter * 32 + lane;
     const uint32_t t_lane = tmem + ((uint32_t)(quarter * 32) << 16);
     int buf = 0;
     uint32_t bphase = 0;
     const int64_t wrow_blocks = (MODE == 1) ? 2 * p.I / 128 : p.H / 128;
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x) {
       ItemCoords c = item_coords(p, item);
+      // rows per warp: 32 (M = 128 item) or 16 (M = 64: lanes 16..31 idle)
+      const int rpw = c.row_end - c.m0 <= 64 ? 16 : 32;
+      const bool lane_ok = lane < rpw;
+      const int r_in_tile = quarter * rpw + lane;
       const int64_t row = c.m0 + r_in_tile;
       // weight scales of the two 128-row blocks of this tile half: gate and up
       // rows (GEMM1) or one W2 row block (GEMM2), one per K block
@@ -239,7 +253,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.f;
       bool ok = true;
-      const bool sa_ok = row < p.Pmax;
+      const bool sa_ok = lane_ok && row < p.Pmax;
       const float *sa_p = p.a_scale + (sa_ok ? row : 0);
       // the scales of K block kb + 1 are loaded while block kb is promoted,
       // so their latency is not on the path between the MMA and the epilogue
@@ -280,7 +294,7 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
       // the item's coordinates again, rather than keeping them in registers
       // through the K loop
       c = item_coords(p, item);
-      const bool valid = row < c.row_end;
+      const bool valid = lane_ok && row < c.row_end;
 
       if (MODE == 1) {
         float amax = 0.f;
@@ -289,18 +303,19 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
           acc[j] = valid ? swiglu(acc[j], acc[64 + j]) : 0.f;  // rows past the segment hold garbage
           amax = fmaxf(amax, fabsf(acc[j]));
         }
-        amax_x[half][r_in_tile] = amax;
+        if (lane_ok) amax_x[half][r_in_tile] = amax;
         named_bar_sync(1, 32 * NUM_EPI_WARPS);
-        const float am = fmaxf(amax_x[0][r_in_tile], amax_x[1][r_in_tile]);
+        const float am = lane_ok ? fmaxf(amax_x[0][r_in_tile], amax_x[1][r_in_tile]) : 0.f;
         named_bar_sync(1, 32 * NUM_EPI_WARPS);
         // The warp's 32 rows go out through its staging buffer: whole boxes
         // by TMA store (asynchronous) when all 32 rows lie in the segment,
         // else the valid rows by plain 16-byte copies from the buffer.
         const int ex = e4m3_block_exponent(am);
         const Pow2 down = pow2_factors(-ex);
-        const int32_t x0 = (int32_t)(c.nb * 128 + half * 64), y0 = (int32_t)(c.m0 + quarter * 32);
-        const int64_t nrows = c.row_end - y0;  // rows of this warp in the segment (may be <= 0)
-        const bool full_q = nrows >= 32;       // warp-uniform
+        const int32_t x0 = (int32_t)(c.nb * 128 + half * 64), y0 = (int32_t)(c.m0 + quarter * rpw);
+        int64_t nrows = c.row_end - y0;  // rows of this warp in the segment (may be <= 0)
+        if (nrows > rpw) nrows = rpw;
+        const bool full_q = nrows == 32;  // warp-uniform
         uint32_t ln;  // opaque copy of the lane index (see the down GEMM's tail)
         asm volatile("mov.u32 %0, %1;" : "=r"(ln) : "r"((uint32_t)lane));
         uint8_t *srow = stg_warp + ln * 32;
@@ -354,9 +369,10 @@ __global__ void __launch_bounds__(THREADS, 1) grouped_gemm_kernel(const __grid_c
         // four 32 x 32 f32 boxes through two 128-byte-swizzled buffers (16-byte
         // piece q of row r sits at piece q ^ (r % 8)): TMA stores when all 32
         // rows of the warp lie in the segment, else plain copies of the valid rows
-        const int32_t y0 = (int32_t)(c.m0 + quarter * 32);
-        const int64_t nrows = c.row_end - y0;
-        const bool full_q = nrows >= 32;  // warp-uniform
+        const int32_t y0 = (int32_t)(c.m0 + quarter * rpw);
+        int64_t nrows = c.row_end - y0;
+        if (nrows > rpw) nrows = rpw;
+        const bool full_q = nrows == 32;  // warp-uniform
         if (lane == 0) bulk_wait_read<0>();
         __syncwarp();
 #pragma unroll
