@@ -37,11 +37,10 @@ constexpr int kTileM = 128;
 
 // Largest split of the router's K loop over CTAs (planes of partial logits).
 constexpr int kRouterMaxKSplit = 8;
-int router_k_split(int64_t T, int64_t E, int64_t H, int sms);
-int router_chain_depth(int64_t T, int64_t H, int ks);
-// gamma_d = d u / (1 - d u) of the logit kernel's longest rounding chain d,
-// rounded up: the relative factor of the router's error bound.
-float router_gamma(int64_t T, int64_t H, int ks);
+int router_chain_depth(int64_t H);
+// gamma_d = d u / (1 - d u) of the small-batch logit kernel's longest
+// rounding chain d, rounded up: the relative factor of its error bound.
+float router_gamma(int64_t H);
 // T <= kRouterWarpMaxT: logits, selection and the pair sort in one launch
 // (ticket: an int32 that is 0 between calls).
 size_t route_decode_smem(int64_t E);
@@ -52,9 +51,17 @@ cudaError_t launch_route_decode(const __nv_bfloat16 *x, int64_t T, const float *
                                 int32_t *perm, int32_t *inv, int32_t *active, int32_t *n_active,
                                 int32_t *tile_offsets, int tile_m, uint32_t *pos_max, int *err,
                                 cudaStream_t s);
-// T > kRouterWarpMaxT: tiled logits (ks planes), then selection.
-cudaError_t launch_router_logits_tiled(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
-                                       int64_t H, int ks, float *logits, float *wnorm, cudaStream_t s);
+// ||W_e||_2 of every router row.
+cudaError_t launch_row_norms(const float *W, int64_t E, int64_t H, float *wnorm, cudaStream_t s);
+// Tensor-core router logits (T > kRouterWarpMaxT): W split into three bf16
+// terms (w_terms [3][E, H], whose map tw has boxes of 128 rows x 64 columns),
+// x through map tx (bf16 [T, H], same boxes); ks planes [ks][T][E].
+bool encode_bf16_tmap(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows);
+int router_tc_k_split(int64_t T, int64_t E, int64_t H, int sms);
+float router_tc_gamma(int64_t H, int ks);
+cudaError_t launch_router_logits_tc(const CUtensorMap &tx, const CUtensorMap &tw, const float *W,
+                                    __nv_bfloat16 *w_terms, int64_t T, int64_t E, int64_t H, int ks,
+                                    float *logits, int *err, int sms, cudaStream_t s);
 cudaError_t launch_x_to_f16(const __nv_bfloat16 *x, int64_t T, int64_t H, __half *x16, float *xscale,
                            cudaStream_t s);
 size_t router_select_smem(int64_t E);

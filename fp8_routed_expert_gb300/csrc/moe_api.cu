@@ -48,6 +48,10 @@ struct moe_ctx {
   float *xss = nullptr;                          // per-(token, 128 columns) sums of squares of x
   int32_t *done13 = nullptr;                     // decode FFN per-tile counters
   int32_t *idle = nullptr;                       // a counter no kernel writes (bounded-wait self-test)
+  __nv_bfloat16 *w_terms = nullptr;              // router W as three bf16 terms (large batches)
+  CUtensorMap tm_rw, tm_rx;                      // maps of w_terms and of the last x
+  const void *tm_rx_ptr = nullptr;               // x and T the map tm_rx describes
+  int64_t tm_rx_T = 0;
   const void *tm_w13_ptr = nullptr, *tm_w2_ptr = nullptr;  // weights the maps in .b describe
   const void *dmaps_w13 = nullptr, *dmaps_w2 = nullptr;    // weights dmaps describe
   int *err = nullptr;
@@ -141,6 +145,26 @@ int resolve_path(const moe_ctx *c, int64_t T) {
   return path;
 }
 
+// Router logits of a large batch (T > kRouterWarpMaxT) on the tensor cores:
+// row norms, the exact bf16 split of W, the logits in *ks planes; *gamma is
+// the relative factor of their error bound.
+int large_batch_logits(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw, int *ks,
+                       float *gamma, cudaStream_t s) {
+  const int64_t E = c->cfg.n_experts, H = c->cfg.hidden;
+  *ks = router_tc_k_split(T, E, H, c->sms);
+  *gamma = router_tc_gamma(H, *ks);
+  if (c->tm_rx_ptr != x || c->tm_rx_T != T) {
+    if (!encode_bf16_tmap(&c->tm_rx, x, H, T)) return MOE_ERR_CUDA;
+    c->tm_rx_ptr = x;
+    c->tm_rx_T = T;
+  }
+  Timed tm(c, MOE_K_ROUTER_LOGITS, s, 3);  // row norms, W split, logits
+  CUDA_TRY(launch_row_norms(rw, E, H, c->wnorm, s));
+  CUDA_TRY(launch_router_logits_tc(c->tm_rx, c->tm_rw, rw, c->w_terms, T, E, H, *ks, c->logits,
+                                   c->err, c->sms, s));
+  return MOE_OK;
+}
+
 // Routing for the grouped-GEMV and grouped-GEMM expert kernels: logits,
 // certified top-k, the pair sort with 128-position tiles; for the GEMV
 // kernels (gemv) also the f16 copy of x with its per-token power-of-two
@@ -148,9 +172,8 @@ int resolve_path(const moe_ctx *c, int64_t T) {
 int route_for_expert_kernels(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw,
                              const float *rb, int k, bool gemv, cudaStream_t s) {
   const int64_t E = c->cfg.n_experts, H = c->cfg.hidden, P = T * k;
-  const int ks = router_k_split(T, E, H, c->sms);
-  const float gamma = router_gamma(T, H, ks);
   if (T <= kRouterWarpMaxT) {
+    const float gamma = router_gamma(H);
     Timed tm(c, MOE_K_ROUTE, s);
     CUDA_TRY(launch_route_decode(x, T, rw, rb, E, H, k, gamma, c->logits, c->wnorm, c->xnorm,
                                  gemv ? c->x16 : nullptr, c->xscale, c->ticket, c->idx, c->wts,
@@ -158,9 +181,11 @@ int route_for_expert_kernels(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, cons
                                  c->tile_offsets, kTileM, gemv ? c->hmax : nullptr, c->err, s));
     return MOE_OK;
   }
+  int ks = 1;
+  float gamma = 0.f;
   {
-    Timed tm(c, MOE_K_ROUTER_LOGITS, s, 2);  // row norms, then the tiled logits
-    CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
+    const int rc = large_batch_logits(c, x, T, rw, &ks, &gamma, s);
+    if (rc != MOE_OK) return rc;
   }
   {
     Timed tm(c, MOE_K_ROUTER_SELECT, s);
@@ -243,15 +268,16 @@ int route_phase(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw, 
                                 c->n_active, c->tile_offsets, kDecodeTileN, c->err, s));
     return MOE_OK;
   }
-  const int ks = router_k_split(T, E, H, c->sms);
+  int ks = 1;
+  float gamma = 0.f;
   {
-    Timed tm(c, MOE_K_ROUTER_LOGITS, s, 2);  // row norms, then the tiled logits
-    CUDA_TRY(launch_router_logits_tiled(x, T, rw, E, H, ks, c->logits, c->wnorm, s));
+    const int rc = large_batch_logits(c, x, T, rw, &ks, &gamma, s);
+    if (rc != MOE_OK) return rc;
   }
   {
     Timed tm(c, MOE_K_ROUTER_SELECT, s);
-    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks,
-                                  router_gamma(T, H, ks), c->idx, c->wts, c->err, s));
+    CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks, gamma, c->idx,
+                                  c->wts, c->err, s));
   }
   {
     Timed tm(c, MOE_K_PERMUTE, s);
@@ -476,6 +502,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->n_active, 16},
       {(void **)&c->ticket, 16},
       {(void **)&c->idle, 16},
+      {(void **)&c->w_terms, Tm > kRouterWarpMaxT ? (size_t)(3 * E * H) * 2 : 16},
       {(void **)&c->done13, (size_t)((Pm + kDecodeTileN - 1) / kDecodeTileN + E + 1) * 4},
       {(void **)&c->xss, (size_t)(Tm * (H / 128)) * 4},
       {(void **)&c->xnorm, (size_t)Tm * 4},
@@ -514,7 +541,8 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
     delete c;
     return MOE_ERR_CUDA;
   }
-  if (!encode_u8_tmap(&c->tm_gemm1.a[0], c->a_hi, H, Pr, 128) ||
+  if ((Tm > kRouterWarpMaxT && !encode_bf16_tmap(&c->tm_rw, c->w_terms, H, 3 * E)) ||
+      !encode_u8_tmap(&c->tm_gemm1.a[0], c->a_hi, H, Pr, 128) ||
       !encode_u8_tmap(&c->tm_gemm1.a[1], c->a_lo, H, Pr, 128) ||
       !encode_u8_tmap(&c->tm_gemm1.a[2], c->a_lo, H, Pr, 128) ||
       !encode_u8_tmap(&c->tm_gemm2.a[0], c->h_t[0], I, Pr, 128) ||

@@ -122,7 +122,7 @@ extern "C" int moe_route_noalloc(const void *hidden, int64_t T, int64_t H, const
   if (cudaMemsetAsync(ticket, 0, 2 * sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
   const cudaError_t e = fp8moe::launch_route_decode(
       static_cast<const __nv_bfloat16 *>(hidden), T, router_w, router_bias, E, H, top_k,
-      fp8moe::router_gamma(T, H, 1), logits, wnorm, xnorm, nullptr, nullptr, ticket, idx, wts,
+      fp8moe::router_gamma(H), logits, wnorm, xnorm, nullptr, nullptr, ticket, idx, wts,
       counts, offsets, perm, inv, active, n_active, tiles, fp8moe::kTileM, nullptr, err, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -744,108 +744,7 @@ __global__ void __launch_bounds__(128) router_select_kernel(SelectArgs a) {
 }
 
 // ------------------------------------------------------------------ logits, T large
-// Tiled SIMT product: a CTA computes 64 tokens x 64 experts, each thread a
-// 4 x 4 block.  Every 32 columns are summed into a fresh partial by a chain
-// of 32 fma; the four partials of a 128-wide K block are added into the
-// block's sum, which is added to the running total: rounding chain length
-// 32 + 4 + H/128 (+ the planes' sum and the bias).  Short chains keep the
-// error bound, and with it the share of tokens sent to the exact path, small.
-__global__ void __launch_bounds__(256) router_logits_tiled_kernel(
-    const __nv_bfloat16 *__restrict__ x, int64_t T, const float *__restrict__ W, int64_t E,
-    int64_t H, float *__restrict__ logits) {
-  // blockIdx.z selects a contiguous range of K blocks; its partial logits go
-  // to plane z of logits [KS][T][E] and the select kernel adds the planes in
-  // order (KS - 1 more roundings in the chain).
-  const int64_t nkb_all = H / 128, ks = gridDim.z, z = blockIdx.z;
-  const int64_t kb_lo = nkb_all * z / ks, kb_hi = nkb_all * (z + 1) / ks;
-  logits += z * T * E;
-  __shared__ __align__(16) float xs[32][68];
-  __shared__ __align__(16) float ws[32][68];
-  const int tid = threadIdx.x;
-  const int tx = tid & 15, ty = tid >> 4;
-  const int64_t t0 = (int64_t)blockIdx.y * 64, e0 = (int64_t)blockIdx.x * 64;
-  float tot[4][4], part[4][4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) tot[i][j] = 0.f;
-
-  const int lr = tid >> 2;        // row of the tile this thread stages (0..63)
-  const int lk = (tid & 3) * 8;   // first of its 8 k values
-  for (int64_t kb = kb_lo * 128; kb < kb_hi * 128; kb += 128) {
-    float blk[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) blk[i][j] = 0.f;
-    for (int kt = 0; kt < 128; kt += 32) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) part[i][j] = 0.f;
-      const int64_t k0 = kb + kt + lk;
-      {
-        float v[8];
-        if (t0 + lr < T) {
-          uint4 xv = __ldg(reinterpret_cast<const uint4 *>(x + (t0 + lr) * H + k0));
-          v[0] = bf16_bits_to_float(xv.x & 0xffffu); v[1] = bf16_bits_to_float(xv.x >> 16);
-          v[2] = bf16_bits_to_float(xv.y & 0xffffu); v[3] = bf16_bits_to_float(xv.y >> 16);
-          v[4] = bf16_bits_to_float(xv.z & 0xffffu); v[5] = bf16_bits_to_float(xv.z >> 16);
-          v[6] = bf16_bits_to_float(xv.w & 0xffffu); v[7] = bf16_bits_to_float(xv.w >> 16);
-        } else {
-#pragma unroll
-          for (int m = 0; m < 8; ++m) v[m] = 0.f;
-        }
-#pragma unroll
-        for (int m = 0; m < 8; ++m) xs[lk + m][lr] = v[m];
-      }
-      {
-        float v[8];
-        if (e0 + lr < E) {
-          float4 a = __ldg(reinterpret_cast<const float4 *>(W + (e0 + lr) * H + k0));
-          float4 b = __ldg(reinterpret_cast<const float4 *>(W + (e0 + lr) * H + k0 + 4));
-          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-        } else {
-#pragma unroll
-          for (int m = 0; m < 8; ++m) v[m] = 0.f;
-        }
-#pragma unroll
-        for (int m = 0; m < 8; ++m) ws[lk + m][lr] = v[m];
-      }
-      __syncthreads();
-#pragma unroll 8
-      for (int kk = 0; kk < 32; ++kk) {
-        float4 a = *reinterpret_cast<const float4 *>(&xs[kk][ty * 4]);
-        float4 b = *reinterpret_cast<const float4 *>(&ws[kk][tx * 4]);
-        float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) part[i][j] = fmaf(av[i], bv[j], part[i][j]);
-      }
-      __syncthreads();
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) blk[i][j] += part[i][j];
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) tot[i][j] += blk[i][j];
-  }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int64_t t = t0 + ty * 4 + i;
-    if (t >= T) continue;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int64_t e = e0 + tx * 4 + j;
-      if (e < E) logits[t * E + e] = tot[i][j];
-    }
-  }
-}
-
+// (the tensor-core kernel in router_tc.cu; the row norms of its bound here)
 // ||W_e||_2, one warp per row.
 __global__ void __launch_bounds__(128) row_norm_kernel(const float *__restrict__ W, int64_t E,
                                                        int64_t H, float *__restrict__ wnorm) {
@@ -866,24 +765,14 @@ __global__ void __launch_bounds__(128) row_norm_kernel(const float *__restrict__
 
 // ------------------------------------------------------------------ launchers
 
-int router_k_split(int64_t T, int64_t E, int64_t H, int sms) {
-  if (T <= kRouterWarpMaxT) return 1;
-  const int64_t tiles = ((T + 63) / 64) * ((E + 63) / 64);
-  int64_t ks = (2 * sms + tiles - 1) / tiles;
-  const int64_t nkb = H / 128;
-  if (ks > nkb) ks = nkb;
-  if (ks > kRouterMaxKSplit) ks = kRouterMaxKSplit;
-  return ks < 1 ? 1 : (int)ks;
-}
+// Longest rounding chain of a logit of the warp-per-expert kernel (T <=
+// kRouterWarpMaxT): lane chain 4 ceil(H / 1024), butterfly 5, sum over the 8
+// warps, bias.  (Large batches use the tensor-core kernel and its own bound.)
+int router_chain_depth(int64_t H) { return (int)(4 * ((H + 1023) / 1024) + 5 + 8 + 1); }
 
-int router_chain_depth(int64_t T, int64_t H, int ks) {
-  return T <= kRouterWarpMaxT ? (int)(4 * ((H + 1023) / 1024) + 5 + 8 + 1)
-                              : (int)(32 + 4 + H / 128 + ks + 1);
-}
-
-float router_gamma(int64_t T, int64_t H, int ks) {
+float router_gamma(int64_t H) {
   const double u = 1.0 / 16777216.0;  // 2^-24
-  const double d = (double)router_chain_depth(T, H, ks);
+  const double d = (double)router_chain_depth(H);
   const double g = d * u / (1.0 - d * u);
   return nextafterf((float)(g * (1.0 + 1e-6)), INFINITY);
 }
@@ -986,13 +875,11 @@ cudaError_t launch_route_small(const __nv_bfloat16 *x, int64_t T, const float *W
   return launch_select_small<32, 8>(r, s);
 }
 
-cudaError_t launch_router_logits_tiled(const __nv_bfloat16 *x, int64_t T, const float *W, int64_t E,
-                                       int64_t H, int ks, float *logits, float *wnorm, cudaStream_t s) {
+cudaError_t launch_row_norms(const float *W, int64_t E, int64_t H, float *wnorm, cudaStream_t s) {
   row_norm_kernel<<<(unsigned)((E + 3) / 4), 128, 0, s>>>(W, E, H, wnorm);
-  dim3 grid((unsigned)((E + 63) / 64), (unsigned)((T + 63) / 64), (unsigned)ks);
-  router_logits_tiled_kernel<<<grid, 256, 0, s>>>(x, T, W, E, H, logits);
   return cudaGetLastError();
 }
+
 
 cudaError_t launch_x_to_f16(const __nv_bfloat16 *x, int64_t T, int64_t H, __half *x16, float *xscale,
                            cudaStream_t s) {
