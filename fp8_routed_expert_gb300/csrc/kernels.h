@@ -65,10 +65,13 @@ cudaError_t launch_router_logits_tc(const CUtensorMap &tx, const CUtensorMap &tw
 cudaError_t launch_x_to_f16(const __nv_bfloat16 *x, int64_t T, int64_t H, __half *x16, float *xscale,
                            cudaStream_t s);
 size_t router_select_smem(int64_t E);
+// queue: one int of device scratch (set to zero on the stream before the
+// launch); warps take tokens from it.
 cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float *W,
                                  const float *bias, int64_t E, int64_t H, int k,
                                  const float *logits, const float *wnorm, int ks, float gamma_d,
-                                 int32_t *idx, float *wts, int *err, cudaStream_t s);
+                                 int32_t *idx, float *wts, int32_t *queue, int *err, int sms,
+                                 cudaStream_t s);
 
 size_t permute_smem(int E);
 // Also clears pos_max[P] (if given) and the n_counters work counters.

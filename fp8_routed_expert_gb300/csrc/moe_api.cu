@@ -190,7 +190,7 @@ int route_for_expert_kernels(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, cons
   {
     Timed tm(c, MOE_K_ROUTER_SELECT, s);
     CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks, gamma, c->idx,
-                                  c->wts, c->err, s));
+                                  c->wts, c->ticket + 1, c->err, c->sms, s));
   }
   if (gemv) {
     c->n_launches += 1;
@@ -277,7 +277,7 @@ int route_phase(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw, 
   {
     Timed tm(c, MOE_K_ROUTER_SELECT, s);
     CUDA_TRY(launch_router_select(x, T, rw, rb, E, H, k, c->logits, c->wnorm, ks, gamma, c->idx,
-                                  c->wts, c->err, s));
+                                  c->wts, c->ticket + 1, c->err, c->sms, s));
   }
   {
     Timed tm(c, MOE_K_PERMUTE, s);

@@ -13,8 +13,8 @@
 // (gamma_d = d u / (1 - d u), u = 2^-24) and Cauchy-Schwarz bounds the sum of
 // |x_h W_eh|.  A token whose selected set and selected order are separated by
 // more than the bounds is certified; otherwise the candidates its bounds cannot
-// rule out are recomputed in f64 from exact products (bf16 x f32 fits in 53
-// bits) and selected again.  This is the "cheap bound first, exact work only
+// rule out are recomputed from exact products, with every rounding error
+// carried (exact_logit), and selected again.  This is the "cheap bound first, exact work only
 // where the bound reaches the best score" pattern of Trochilus's output head
 // ("What makes it different").
 #include <climits>
@@ -100,29 +100,62 @@ __device__ __forceinline__ void x_to_f16(const __nv_bfloat16 *xt, int64_t H, flo
   if (lane == 0) *xscale_t = exp2i(sh);
 }
 
-// logit of expert e for x_t in f64 from exact products (bf16 x f32 fits in 53
-// bits), by the whole warp; four loads per lane in flight.
+// Error-free f32 steps for the exact logits: x * w = p + q exactly (p the
+// rounded product, q = fma(x, w, -p)), and a + b = s + err exactly (Knuth's
+// TwoSum).  The _rn intrinsics keep the compiler from contracting or
+// reordering them.
+__device__ __forceinline__ void two_prod(float x, float w, float &p, float &q) {
+  p = __fmul_rn(x, w);
+  q = fmaf(x, w, -p);
+}
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &err) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// Adds x * w into the unevaluated sum hi + lo.
+__device__ __forceinline__ void acc_exact(float x, float w, float &hi, float &lo) {
+  float p, q, s, e;
+  two_prod(x, w, p, q);
+  two_sum(hi, p, s, e);
+  hi = s;
+  lo = __fadd_rn(lo, __fadd_rn(e, q));
+}
+
+// logit of expert e for x_t, by the whole warp, from exact products: every
+// product and every addition's rounding error is carried in f32 pairs (hi +
+// lo, eight independent chains per lane), whose sum in f64 differs from the
+// exact dot product by at most about n^2 2^-48 of sum |x W| (n = H / 256
+// products per chain: 2e-12 of it at H = 6144, 3.7e-12 at H = 8192).  The
+// f32 pipes are many times wider than the f64 one; eight loads per lane are
+// in flight.
 __device__ __forceinline__ double exact_logit(const SelectArgs &a, const __nv_bfloat16 *xt, int e) {
   const int lane = threadIdx.x & 31;
   const float *w = a.W + (int64_t)e * a.H;
-  double acc[4] = {0.0, 0.0, 0.0, 0.0};  // independent chains: the f64 pipe is slow
-  for (int64_t h0 = 4 * lane; h0 < a.H; h0 += 512) {
-    float4 wv[4];
-    uint2 xv[4];
+  constexpr int U = 8;  // loads per lane in flight (chains)
+  float hi[U], lo[U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+  for (int u = 0; u < U; ++u) hi[u] = lo[u] = 0.f;
+  for (int64_t h0 = 4 * lane; h0 < a.H; h0 += 128 * U) {
+    float4 wv[U];
+    uint2 xv[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
       const int64_t h = h0 + 128 * u;
       wv[u] = h < a.H ? __ldg(reinterpret_cast<const float4 *>(w + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
       xv[u] = h < a.H ? __ldg(reinterpret_cast<const uint2 *>(xt + h)) : make_uint2(0u, 0u);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc[u] = fma((double)bf16_bits_to_float(xv[u].x & 0xffffu), (double)wv[u].x, acc[u]);
-      acc[u] = fma((double)bf16_bits_to_float(xv[u].x >> 16), (double)wv[u].y, acc[u]);
-      acc[u] = fma((double)bf16_bits_to_float(xv[u].y & 0xffffu), (double)wv[u].z, acc[u]);
-      acc[u] = fma((double)bf16_bits_to_float(xv[u].y >> 16), (double)wv[u].w, acc[u]);
+    for (int u = 0; u < U; ++u) {
+      acc_exact(bf16_bits_to_float(xv[u].x & 0xffffu), wv[u].x, hi[u], lo[u]);
+      acc_exact(bf16_bits_to_float(xv[u].x >> 16), wv[u].y, hi[u], lo[u]);
+      acc_exact(bf16_bits_to_float(xv[u].y & 0xffffu), wv[u].z, hi[u], lo[u]);
+      acc_exact(bf16_bits_to_float(xv[u].y >> 16), wv[u].w, hi[u], lo[u]);
     }
   }
+  double acc[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) acc[u] = ((double)hi[u] + (double)lo[u]) + ((double)hi[u + 4] + (double)lo[u + 4]);
   double v = warp_sum((acc[0] + acc[1]) + (acc[2] + acc[3]));
   if (a.bias != nullptr) v += (double)a.bias[e];
   return v;
@@ -206,9 +239,9 @@ __device__ __noinline__ void select_token(const SelectArgs &a, int64_t t, float 
   // largest lower bound (the others are certainly below k experts).  A
   // candidate whose interval [l - beta, l + beta] overlaps no other
   // candidate's is "isolated": its f32 value already orders it correctly
-  // against every candidate.  Only the others are recomputed in f64 from exact
-  // products; the top k is then taken on key = f64 value (recomputed) or f32
-  // value (isolated), which orders every pair of candidates exactly.
+  // against every candidate.  Only the others are recomputed from exact
+  // products (exact_logit); the top k is then taken on key = recomputed value
+  // or f32 value (isolated), which orders every pair of candidates exactly.
   uint32_t taken2 = 0;
   float kth_lo = -INFINITY;
   auto lo_key = [&](int e) -> float { return key32(e) - beta(e); };
@@ -731,16 +764,24 @@ __global__ void __launch_bounds__(128) x_to_f16_kernel(const __nv_bfloat16 *__re
 
 // ------------------------------------------------------------------ selection, T large
 // One warp per token.  Shared memory per warp: E floats and E doubles.
-__global__ void __launch_bounds__(128) router_select_kernel(SelectArgs a) {
+// Warps take tokens from a global counter (zero at launch): a token whose
+// selection needs the exact path costs many times a certified one, and
+// those tokens fall unevenly, so a fixed token-to-warp map would leave the
+// run as long as its most loaded SM.
+__global__ void __launch_bounds__(128) router_select_kernel(SelectArgs a, int32_t *queue) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int64_t t = (int64_t)blockIdx.x * nw + wid;
+  const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5, lane = threadIdx.x & 31;
   double *lg64 = reinterpret_cast<double *>(smem_raw) + (size_t)wid * a.E;
   float *lg = reinterpret_cast<float *>(smem_raw + (size_t)nw * a.E * sizeof(double)) + (size_t)wid * 2 * a.E;
-  if (t >= a.T) return;
-  float xn, amax;
-  x_stats(a.x + t * a.H, a.H, &xn, &amax);
-  select_token(a, t, xn, lg, lg + a.E, lg64);
+  while (true) {
+    int64_t t = 0;
+    if (lane == 0) t = atomicAdd(queue, 1);
+    t = __shfl_sync(0xffffffffu, t, 0);
+    if (t >= a.T) break;
+    float xn, amax;
+    x_stats(a.x + t * a.H, a.H, &xn, &amax);
+    select_token(a, t, xn, lg, lg + a.E, lg64);
+  }
 }
 
 // ------------------------------------------------------------------ logits, T large
@@ -892,7 +933,8 @@ size_t router_select_smem(int64_t E) { return (size_t)4 * E * (sizeof(double) + 
 cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float *W,
                                  const float *bias, int64_t E, int64_t H, int k,
                                  const float *logits, const float *wnorm, int ks, float gamma_d,
-                                 int32_t *idx, float *wts, int *err, cudaStream_t s) {
+                                 int32_t *idx, float *wts, int32_t *queue, int *err, int sms,
+                                 cudaStream_t s) {
   SelectArgs a = select_args(x, T, W, bias, E, H, k, logits, ks, wnorm, gamma_d, idx, wts, err);
   const size_t smem = router_select_smem(E);
   if (smem > 48 * 1024) {
@@ -900,7 +942,16 @@ cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  router_select_kernel<<<(unsigned)((T + 3) / 4), 128, smem, s>>>(a);
+  int per_sm = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, router_select_kernel, 128, smem) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  int64_t grid = (T + 3) / 4;
+  if (grid > (int64_t)sms * per_sm) grid = (int64_t)sms * per_sm;
+  if (grid <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(queue, 0, sizeof(int32_t), s);
+  if (e != cudaSuccess) return e;
+  router_select_kernel<<<(unsigned)grid, 128, smem, s>>>(a, queue);
   return cudaGetLastError();
 }
 

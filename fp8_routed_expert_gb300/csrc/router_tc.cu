@@ -7,7 +7,7 @@
 // f32, and the three terms are summed by tcgen05.mma kind::f16 (bf16 x bf16,
 // f32 accumulate) into one TMEM accumulator.  To keep the rounding chain of
 // every logit short -- its length enters the error bound that certifies the
-// top-k selection (the exact f64 path takes the tokens it cannot certify) --
+// top-k selection (the exact path takes the tokens it cannot certify) --
 // each 128-wide K block is accumulated in its own TMEM buffer (24 MMA
 // instructions) and added to f32 registers by the epilogue, K blocks in
 // ascending order; a K range split over CTAs lands in separate planes that

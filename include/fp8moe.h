@@ -92,7 +92,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg);
  * T = 0 is a no-op.  Routing is exact: indices, counts and the permutation
  * equal those of exact arithmetic on the inputs (f32 logits carry a rigorous
  * error bound; tokens whose order the bound cannot certify are recomputed
- * in f64).  Device-side failures (a bounded wait that gave up, a non-finite
+ * from exact products with every rounding error carried).  Device-side failures (a bounded wait that gave up, a non-finite
  * logit) are recorded in the context and reported by moe_status.
  */
 int moe_layer_forward(moe_ctx *ctx, const void *hidden, int64_t T, const float *router_w,
