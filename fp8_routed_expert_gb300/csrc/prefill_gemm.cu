@@ -490,7 +490,8 @@ __device__ __forceinline__ void quant_row_2terms(const __nv_bfloat16 *__restrict
 
 // Position rows: row pos is x of token perm[pos] / k (the expert-sorted
 // operand of the grouped GEMM); scales a_scale[kb * Pmax + pos].
-__global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16 *__restrict__ x,
+// (four CTAs per SM: the row loop is bound by latency, not by registers)
+__global__ void __launch_bounds__(256, 4) act_quant_kernel(const __nv_bfloat16 *__restrict__ x,
                                                         const int32_t *__restrict__ perm, int64_t P,
                                                         int k, int64_t H, int64_t Pmax,
                                                         uint8_t *__restrict__ a_hi,
