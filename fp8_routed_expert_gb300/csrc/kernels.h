@@ -74,11 +74,16 @@ cudaError_t launch_router_select(const __nv_bfloat16 *x, int64_t T, const float 
                                  cudaStream_t s);
 
 size_t permute_smem(int E);
-// Also clears pos_max[P] (if given) and the n_counters work counters.
+// Chunks of the many-CTA sort for P pairs (chunk_hist needs chunks x E ints).
+int64_t permute_chunks(int64_t P);
+// Also clears pos_max[P] (if given) and the n_counters work counters.  With
+// chunk_hist (device scratch of permute_chunks(P) x E ints) and more than two
+// chunks the sort runs over many CTAs; otherwise in one CTA.
 cudaError_t launch_permute(const int32_t *idx, int64_t P, int E, int tile_m, int32_t *counts,
                            int32_t *offsets, int32_t *perm, int32_t *inv, int32_t *active,
                            int32_t *n_active, int32_t *tile_offsets, uint32_t *pos_max,
-                           int32_t *counters, int n_counters, int *err, cudaStream_t s);
+                           int32_t *counters, int n_counters, int *err, cudaStream_t s,
+                           int32_t *chunk_hist = nullptr);
 
 // Decode grouped GEMVs over the active experts' weight rows; T bounds the
 // tokens any expert can hold (passes of 64 tokens above 64).

@@ -47,6 +47,7 @@ struct moe_ctx {
   DecodeMaps dmaps;                              // tensor-core decode FFN operands
   float *xss = nullptr;                          // per-(token, 128 columns) sums of squares of x
   int32_t *done13 = nullptr;                     // decode FFN per-tile counters
+  int32_t *chunk_hist = nullptr;                 // many-CTA pair sort: [chunks][E]
   int32_t *idle = nullptr;                       // a counter no kernel writes (bounded-wait self-test)
   __nv_bfloat16 *w_terms = nullptr;              // router W as three bf16 terms (large batches)
   CUtensorMap tm_rw, tm_rx;                      // maps of w_terms and of the last x
@@ -197,10 +198,10 @@ int route_for_expert_kernels(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, cons
     CUDA_TRY(launch_x_to_f16(x, T, H, c->x16, c->xscale, s));
   }
   {
-    Timed tm(c, MOE_K_PERMUTE, s);
+    Timed tm(c, MOE_K_PERMUTE, s, permute_chunks(P) > 2 ? 3 : 1);  // many-CTA sort above two chunks
     CUDA_TRY(launch_permute(c->idx, P, (int)E, kTileM, c->counts, c->offsets, c->perm, c->inv,
                             c->active, c->n_active, c->tile_offsets, gemv ? c->hmax : nullptr,
-                            nullptr, 0, c->err, s));
+                            nullptr, 0, c->err, s, c->chunk_hist));
   }
   return MOE_OK;
 }
@@ -280,10 +281,10 @@ int route_phase(moe_ctx *c, const __nv_bfloat16 *x, int64_t T, const float *rw, 
                                   c->wts, c->ticket + 1, c->err, c->sms, s));
   }
   {
-    Timed tm(c, MOE_K_PERMUTE, s);
+    Timed tm(c, MOE_K_PERMUTE, s, permute_chunks(P) > 2 ? 3 : 1);  // many-CTA sort above two chunks
     CUDA_TRY(launch_permute(c->idx, P, (int)E, kDecodeTileN, c->counts, c->offsets, c->perm,
                             c->inv, c->active, c->n_active, c->tile_offsets, nullptr, c->done13,
-                            (int)max_tiles + 1, c->err, s));
+                            (int)max_tiles + 1, c->err, s, c->chunk_hist));
   }
   {
     Timed tm(c, MOE_K_ACT_QUANT, s);
@@ -504,6 +505,7 @@ int moe_init(moe_ctx **out, const moe_config *cfg) {
       {(void **)&c->idle, 16},
       {(void **)&c->w_terms, Tm > kRouterWarpMaxT ? (size_t)(3 * E * H) * 2 : 16},
       {(void **)&c->done13, (size_t)((Pm + kDecodeTileN - 1) / kDecodeTileN + E + 1) * 4},
+      {(void **)&c->chunk_hist, (size_t)(permute_chunks(Pm) * E) * 4},
       {(void **)&c->xss, (size_t)(Tm * (H / 128)) * 4},
       {(void **)&c->xnorm, (size_t)Tm * 4},
       {(void **)&c->tile_offsets, (size_t)(E + 1) * 4},
