@@ -58,9 +58,11 @@ def test_olmoe_decode(T, path):
     check_output(out, ref)
 
 
-@pytest.mark.parametrize("T", [2, 17, 64, 65, 127, 129, 300])
+@pytest.mark.parametrize("T", [2, 17, 64, 65, 127, 129, 300, 513])
 def test_olmoe_ragged_batches(T):
-    """Batches that straddle the GEMV/GEMM switch and the 128-row tiles."""
+    """Batches that straddle the GEMV/GEMM switch and the 128-row tiles; T =
+    513 (4104 pairs) also the one-CTA / many-CTA switch of the pair sort, with
+    a last chunk of 8 pairs."""
     fam, w, dw = weights("olmoe_decode")
     x = W.make_x(fam, T)
     layer = make_layer(fam, T)
