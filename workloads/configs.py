@@ -58,6 +58,10 @@ FAMILIES = {
     "wide_decode": Family("wide_decode", 4096, 384, 6, 2048, 4, (1, 16, 64)),
     "large_prefill": Family("large_prefill", 6144, 512, 12, 2048, 5, (4096,), bias_std=1.0),
     "dense_ffn": Family("dense_ffn", 2048, 1, 1, 8192, 6, (8, 2048)),
+    # the large prefill batch's router and tokens (same seed) with I = 128
+    # experts: profiles of the routing kernels within about 1 GB of device
+    # memory
+    "large_router": Family("large_router", 6144, 512, 12, 128, 5, (4096,), bias_std=1.0),
 }
 
 # tensor ids of the counter-based streams
